@@ -1,0 +1,306 @@
+"""Pins for the fp64 oracle, checked against what the pages and mathematics fix.
+
+Nothing here compares the oracle with itself or retypes its formula: each
+check is a value the pages print, a closed form, an invariant of the exact
+function, or a separately written high-precision brute force (Python
+``decimal`` at 40 digits, softmax taken without max subtraction).  A dropped
+term, a wrong sign or index, a transposed operand or a wrong causal direction
+in the oracle fails at least one of them.
+"""
+import math
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import read_golden
+
+
+# ---------------------------------------------------------------- page values
+def test_worked_example_dense_and_blockwise():
+    """wpnews.pro "Understanding FlashAttention Pt 1", section 2.5."""
+    g = read_golden("wpnews_s2_5_worked_example.txt")
+    s = np.array(g["scores"])
+    v = np.array(g["v"])
+    tol = g["tol"][0]
+    # d = 1, q = [1], k_j = [s_j], scale 1: the scaled score row is s itself.
+    q = np.ones((1, 1, 1))[:, :, :].repeat(len(s), axis=1)  # every query row = [1]
+    k = s.reshape(1, -1, 1)
+    vv = v.reshape(1, len(s), 2)
+    O, L = oracle.attention_fwd(q, k, vv, causal=False, scale=1.0, rows=[0])
+    np.testing.assert_allclose(O[0, 0], g["o"], atol=tol, rtol=0)
+    # LSE = m + log(l) with the printed m and l
+    assert abs(L[0, 0] - (g["max"][0] + math.log(g["ell"][0]))) < tol
+
+    split = int(g["block_split"][0])
+    bounds = [0, split, len(s)]
+    Ob, Lb, M, Lsum, A = oracle.attention_fwd_blockwise(
+        q, k, vv, bounds, scale=1.0, rows=[0], return_state=True)
+    np.testing.assert_allclose(Ob[0, 0], g["o"], atol=tol, rtol=0)
+    assert abs(Lsum[0, 0] - g["ell"][0]) < tol
+    assert M[0, 0] == g["max"][0]
+    np.testing.assert_allclose(A[0, 0], g["a2"], atol=tol, rtol=0)
+
+    # state after block 1 alone: m_1 = 2, l_1 = 1 + e^{-1}
+    _, _, M1, L1, A1 = oracle.attention_fwd_blockwise(
+        q[:, :split], k[:, :split], vv[:, :split], [0, split], scale=1.0,
+        rows=[0], return_state=True)
+    assert M1[0, 0] == g["block1_max"][0]
+    assert abs(L1[0, 0] - g["block1_ell"][0]) < tol
+    # alpha = e^{m_1 - m_2} takes block 1's state to block 2's reference
+    alpha = math.exp(g["block2_alpha_exp"][0])
+    assert abs(alpha * L1[0, 0] + 1 + math.exp(-1) - g["ell"][0]) < tol
+
+
+def test_overflow_example_stays_finite():
+    """wpnews.pro section 2.2: [1000, 999] must not overflow."""
+    g = read_golden("wpnews_s2_2_overflow.txt")
+    s = np.array(g["scores"])
+    q = np.ones((1, 2, 1))
+    k = s.reshape(1, 2, 1)
+    v = np.eye(2).reshape(1, 2, 2)  # O row = the softmax weights
+    O, L = oracle.attention_fwd(q, k, v, scale=1.0, rows=[0])
+    assert np.all(np.isfinite(O)) and np.isfinite(L).all()
+    w = np.array(g["weights_printed"])
+    np.testing.assert_allclose(O[0, 0], w / w.sum(), atol=g["tol_printed"][0])
+    # closed form: weights [1, e^-1]/(1+e^-1), LSE = 1000 + log(1 + e^-1)
+    e = math.exp(-1)
+    np.testing.assert_allclose(O[0, 0], [1 / (1 + e), e / (1 + e)], atol=1e-15)
+    assert abs(L[0, 0] - (1000 + math.log1p(e))) < 1e-12
+    Ob, Lb = oracle.attention_fwd_blockwise(q, k, v, [0, 1, 2], scale=1.0, rows=[0])
+    np.testing.assert_allclose(Ob, O, atol=1e-15)
+    assert abs(Lb[0, 0] - L[0, 0]) < 1e-12
+
+
+# ---------------------------------------------------------------- brute force
+def _brute(q, k, v, causal, scale):
+    """Direct softmax in 40-digit decimals: p_ij = exp(s_ij) / sum exp(s_ik)."""
+    getcontext().prec = 40
+    N, d = q.shape
+    dv = v.shape[1]
+    O = np.zeros((N, dv))
+    L = np.zeros(N)
+    sc = Decimal(repr(float(scale)))
+    for i in range(N):
+        keys = [j for j in range(N) if (not causal or j <= i)]
+        e = {}
+        for j in keys:
+            s = sum(Decimal(repr(float(q[i, c]))) * Decimal(repr(float(k[j, c])))
+                    for c in range(d)) * sc
+            e[j] = s.exp()
+        z = sum(e.values())
+        for c in range(dv):
+            O[i, c] = float(sum(e[j] * Decimal(repr(float(v[j, c]))) for j in keys) / z)
+        L[i] = float(z.ln())
+    return O, L
+
+
+@pytest.mark.parametrize("N,d,dv,causal,seed", [
+    (1, 1, 1, False, 0), (2, 3, 2, True, 1), (5, 4, 3, False, 2),
+    (7, 2, 4, True, 3), (8, 4, 4, False, 4), (8, 4, 4, True, 5),
+])
+def test_brute_force_tiny(N, d, dv, causal, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((N, d)) * 1.5
+    k = rng.standard_normal((N, d)) * 1.5 + 0.25  # asymmetric: q/k swap shows
+    v = rng.standard_normal((N, dv))
+    scale = 0.7
+    Ob, Lb = _brute(q, k, v, causal, scale)
+    O, L = oracle.attention_fwd(q[None], k[None], v[None], causal=causal, scale=scale)
+    np.testing.assert_allclose(O[0], Ob, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(L[0], Lb, atol=1e-13, rtol=0)
+    # rows mode gives the same rows
+    rows = np.arange(N)[::-1].copy()
+    Or, Lr = oracle.attention_fwd(q[None], k[None], v[None], causal=causal,
+                                  scale=scale, rows=rows)
+    np.testing.assert_allclose(Or[0], Ob[::-1], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(Lr[0], Lb[::-1], atol=1e-13, rtol=0)
+
+
+def test_toy_8_tokens_d4_tiles4():
+    """tokentrails.org "FlashAttention": 8 tokens, d = 4, 4 x 4 tiles,
+    checked against ordinary attention."""
+    rng = np.random.default_rng(8)
+    q, k, v = (rng.standard_normal((1, 8, 4)) for _ in range(3))
+    for causal in (False, True):
+        Ob, Lb = _brute(q[0], k[0], v[0], causal, 0.5)
+        Ot, Lt = oracle.attention_fwd_blockwise(q, k, v, [0, 4, 8], causal=causal)
+        np.testing.assert_allclose(Ot[0], Ob, atol=1e-13)
+        np.testing.assert_allclose(Lt[0], Lb, atol=1e-13)
+
+
+# ------------------------------------------------------- closed forms, invariants
+def _rand(rng, BH, N, d, dv=None):
+    dv = dv or d
+    return (rng.standard_normal((BH, N, d)), rng.standard_normal((BH, N, d)),
+            rng.standard_normal((BH, N, dv)))
+
+
+def test_identical_keys_give_mean_of_v():
+    rng = np.random.default_rng(11)
+    q, _, v = _rand(rng, 3, 37, 16)
+    k = np.broadcast_to(rng.standard_normal((3, 1, 16)), (3, 37, 16)).copy()
+    scale = 0.25
+    O, L = oracle.attention_fwd(q, k, v, scale=scale)
+    np.testing.assert_allclose(O, np.broadcast_to(v.mean(axis=1, keepdims=True), O.shape),
+                               atol=1e-13)
+    s = scale * np.einsum("bnd,bd->bn", q, k[:, 0])
+    np.testing.assert_allclose(L, s + math.log(37), atol=1e-12)
+
+
+def test_single_key_returns_v():
+    rng = np.random.default_rng(12)
+    q, k, v = _rand(rng, 4, 1, 8, 5)
+    O, L = oracle.attention_fwd(q, k, v, scale=0.3)
+    np.testing.assert_array_equal(O, v)
+    np.testing.assert_allclose(L[:, 0], 0.3 * np.einsum("bd,bd->b", q[:, 0], k[:, 0]),
+                               atol=1e-14)
+
+
+def test_causal_first_row_returns_v0():
+    rng = np.random.default_rng(13)
+    q, k, v = _rand(rng, 2, 33, 8)
+    O, L = oracle.attention_fwd(q, k, v, causal=True, scale=0.5)
+    np.testing.assert_allclose(O[:, 0], v[:, 0], atol=1e-15)
+    np.testing.assert_allclose(L[:, 0], 0.5 * np.einsum("bd,bd->b", q[:, 0], k[:, 0]),
+                               atol=1e-14)
+    # causal output of row i equals non-causal attention over keys 0..i
+    for i in (1, 7, 32):
+        Oi, Li = oracle.attention_fwd(q[:, :i + 1], k[:, :i + 1], v[:, :i + 1],
+                                      scale=0.5, rows=[i])
+        np.testing.assert_allclose(O[:, i], Oi[:, 0], atol=1e-14)
+        np.testing.assert_allclose(L[:, i], Li[:, 0], atol=1e-13)
+
+
+def test_rows_of_p_sum_to_one_and_value_shift():
+    """sum_j P_ij = 1  <=>  adding c to every value row adds c to O."""
+    rng = np.random.default_rng(14)
+    q, k, v = _rand(rng, 2, 50, 8, 6)
+    for causal in (False, True):
+        O, _ = oracle.attention_fwd(q, k, v, causal=causal)
+        ones, _ = oracle.attention_fwd(q, k, np.ones_like(v), causal=causal)
+        np.testing.assert_allclose(ones, 1.0, atol=1e-14)
+        c = rng.standard_normal(6)
+        O2, _ = oracle.attention_fwd(q, k, v + c, causal=causal)
+        np.testing.assert_allclose(O2, O + c, atol=1e-13)
+
+
+def test_key_value_permutation_invariance():
+    rng = np.random.default_rng(15)
+    q, k, v = _rand(rng, 2, 41, 8)
+    perm = rng.permutation(41)
+    O, L = oracle.attention_fwd(q, k, v)
+    Op, Lp = oracle.attention_fwd(q, k[:, perm], v[:, perm])
+    np.testing.assert_allclose(Op, O, atol=1e-13)
+    np.testing.assert_allclose(Lp, L, atol=1e-13)
+    # permuting keys without values must change O (catches a K/V mix-up)
+    Ox, _ = oracle.attention_fwd(q, k[:, perm], v)
+    assert np.abs(Ox - O).max() > 1e-3
+
+
+def test_key_shift_moves_lse_only():
+    rng = np.random.default_rng(16)
+    q, k, v = _rand(rng, 2, 29, 8)
+    u = rng.standard_normal(8)
+    scale = 0.4
+    O, L = oracle.attention_fwd(q, k, v, scale=scale)
+    O2, L2 = oracle.attention_fwd(q, k + u, v, scale=scale)
+    np.testing.assert_allclose(O2, O, atol=1e-13)
+    np.testing.assert_allclose(L2, L + scale * np.einsum("bnd,d->bn", q, u), atol=1e-12)
+
+
+def test_scale_enters_as_multiplier():
+    """scale * (q . k): doubling q at half the scale changes nothing."""
+    rng = np.random.default_rng(17)
+    q, k, v = _rand(rng, 1, 23, 8)
+    O, L = oracle.attention_fwd(q, k, v, scale=0.6)
+    O2, L2 = oracle.attention_fwd(2 * q, k, v, scale=0.3)
+    np.testing.assert_allclose(O2, O, atol=1e-14)
+    np.testing.assert_allclose(L2, L, atol=1e-13)
+    # and the scale really matters
+    O3, _ = oracle.attention_fwd(q, k, v, scale=1.2)
+    assert np.abs(O3 - O).max() > 1e-3
+
+
+# --------------------------------------------------------- blockwise == dense
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_blockwise_equals_dense_any_split(causal, reverse):
+    """Blockwise online softmax equals the dense result for any split,
+    including uneven blocks (gowda.ai Exercise 26.4) and, for causal rows
+    visited last block first, blocks that are entirely masked."""
+    rng = np.random.default_rng(18 + 2 * causal + reverse)
+    N = 61
+    q, k, v = _rand(rng, 2, N, 8, 5)
+    q *= 2.0  # spread the scores so the running max moves often
+    O, L = oracle.attention_fwd(q, k, v, causal=causal)
+    splits = [[0, N], [0, 1, N], [0, 13, 14, 40, N], list(range(0, N, 4)) + [N],
+              list(range(N + 1))]
+    for _ in range(5):
+        cuts = sorted(set(rng.integers(1, N, size=rng.integers(1, 9)).tolist()))
+        splits.append([0] + cuts + [N])
+    for b in splits:
+        Ob, Lb = oracle.attention_fwd_blockwise(q, k, v, b, causal=causal,
+                                                reverse=reverse)
+        np.testing.assert_allclose(Ob, O, atol=1e-13, rtol=0)
+        np.testing.assert_allclose(Lb, L, atol=1e-12, rtol=0)
+
+
+def test_blockwise_late_max_moves():
+    """Scores that grow along the row make the running max move at every
+    block: the rescale must be applied to both l and the accumulator."""
+    N = 32
+    q = np.ones((1, N, 1))
+    k = np.linspace(-3, 9, N).reshape(1, N, 1)
+    v = np.random.default_rng(19).standard_normal((1, N, 3))
+    O, L = oracle.attention_fwd(q, k, v, scale=1.0)
+    Ob, Lb = oracle.attention_fwd_blockwise(q, k, v, list(range(0, N + 1, 3)) + [N]
+                                            if N % 3 else list(range(0, N + 1, 3)),
+                                            scale=1.0)
+    np.testing.assert_allclose(Ob, O, atol=1e-13)
+    np.testing.assert_allclose(Lb, L, atol=1e-12)
+
+
+# ------------------------------------------------------------ degenerate cases
+def test_fully_masked_row_is_defined():
+    """No key allowed: defined as O = 0, LSE = -inf, never NaN (blockwise
+    guard); reachable only through the blockwise reverse order per block."""
+    q = np.ones((1, 3, 2))
+    k = np.ones((1, 3, 2))
+    v = np.ones((1, 3, 2))
+    # a block that lies entirely above the diagonal for row 0
+    _, _, M, Lsum, A = oracle.attention_fwd_blockwise(
+        q[:, :3], k, v, [0, 1, 3], causal=True, reverse=True, rows=[0],
+        return_state=True)
+    assert M[0, 0] == 2.0 / math.sqrt(2) and Lsum[0, 0] == 1.0
+    np.testing.assert_array_equal(A[0, 0], [1.0, 1.0])
+
+
+def test_bf16_conversion_is_exact():
+    bits = np.array([0x3F80, 0xC000, 0x0001, 0x7F80, 0xFF80, 0x3F81, 0x0000, 0x8000,
+                     0x4049], dtype=np.uint16)
+    want = [1.0, -2.0, 2.0 ** -133, math.inf, -math.inf, 1.0 + 2.0 ** -7, 0.0, -0.0,
+            3.140625]
+    got = oracle.bf16_bits_to_f64(bits)
+    np.testing.assert_array_equal(got, want)
+    assert math.copysign(1.0, got[7]) == -1.0
+
+
+def test_thread_count_does_not_change_results():
+    rng = np.random.default_rng(20)
+    q, k, v = _rand(rng, 5, 130, 16)
+    a = oracle.attention_fwd(q, k, v, causal=True, nthreads=1)
+    b = oracle.attention_fwd(q, k, v, causal=True, nthreads=7)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_bad_arguments_rejected():
+    q = np.ones((1, 4, 2))
+    with pytest.raises(ValueError):
+        oracle.attention_fwd(q, q, q, rows=[4])
+    with pytest.raises(ValueError):
+        oracle.attention_fwd_blockwise(q, q, q, [0, 2, 2, 4])
+    with pytest.raises(ValueError):
+        oracle.attention_fwd_blockwise(q, q, q, [0, 3])
