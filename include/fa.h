@@ -1,0 +1,141 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward pass.
+ *
+ *   O   = softmax(scale * Q K^T [+ causal mask]) V
+ *   LSE = m + log(l)          (per query row, natural log)
+ *
+ * The operation: "Chapter 26 Online Softmax & FlashAttention" (gowda.ai),
+ * section 26.2 and Listing 26.2 (scores q k^T / sqrt(d), causal keeps key j
+ * for query i iff j <= i, stable row softmax, weights @ v); the logsumexp
+ * statistic L = m + log(l) is "Fix 2" of "FlashAttention-2 -- Deeper Math"
+ * (aicassindra.com).  The kernel computes it exactly (no approximation)
+ * with the online-softmax recurrence of "Understanding FlashAttention Pt 1"
+ * (wpnews.pro), section 2.4, query blocks outermost ("Fix 3"), one CTA per
+ * (batch, head, query block) ("Fix 4"), and causal tiles above the diagonal
+ * skipped ("Causal masking: skip the blocks, do not mask them").
+ *
+ * Every entry point returns an fa_status (0 = success, negative = error).
+ * No entry point falls back to another implementation: an unsupported
+ * argument is an error code.  Nothing here is thread-hostile; concurrent
+ * calls on different streams are independent.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; identical to cudaStream_t / CUstream.  NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,        /* a required pointer is NULL */
+    FA_ERR_SHAPE = -2,       /* B, H or N < 1, or a size overflows the indexing */
+    FA_ERR_HEADDIM = -3,     /* d is not 64 or 128 */
+    FA_ERR_ALIGN = -4,       /* Q, K, V, O not 16-byte aligned, or LSE not 4-byte */
+    FA_ERR_ARCH = -5,        /* current device is not compute capability 10.3 */
+    FA_ERR_LAUNCH = -6,      /* a CUDA call failed (launch, copy, tensor map) */
+    FA_ERR_TIMEOUT = -7,     /* a kernel wait exceeded its limit (see fa_device_error) */
+    FA_ERR_UNSUPPORTED = -8, /* valid request this build does not implement */
+    FA_ERR_SCALE = -9,       /* scale is not a finite number > 0 */
+    FA_ERR_ALIAS = -10,      /* an output buffer overlaps an input buffer */
+    FA_ERR_WORKSPACE = -11   /* workspace too small or misaligned */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward on device buffers, enqueued on `stream`.
+ *
+ *   Q, K, V  bf16 [B, H, N, d], contiguous, device memory; element
+ *            (b, h, n, k) at ((b*H + h)*N + n)*d + k.  Read only.
+ *   O        bf16 [B, H, N, d], same layout, device memory, written.
+ *   LSE      fp32 [B, H, N], device memory, written: log(sum_j exp(s_ij))
+ *            over the scaled, masked scores s_ij = scale * q_i . k_j.
+ *   B, H, N  >= 1.  B*H < 2^31, N < 2^31.
+ *   d        64 or 128 (head dimension; values have the same width).
+ *   causal   0: every key; nonzero: key j is used for query i iff j <= i.
+ *   scale    finite, > 0; the pages' choice is 1/sqrt(d).
+ *
+ * All buffers are owned by the caller; the library keeps no pointer after
+ * the call and allocates no device memory.  Q, K, V, O must be 16-byte
+ * aligned, LSE 4-byte aligned, and O / LSE must not overlap Q, K or V.
+ * Arguments are checked on the host before any CUDA call; on error nothing
+ * is enqueued.  The kernel runs asynchronously: a FA_OK return means it was
+ * enqueued, and fa_device_error() reports a failure found while it ran.
+ * Results are deterministic: the same inputs give bit-identical outputs.
+ */
+int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+           int B, int H, int N, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
+ * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs for this
+ * shape: room for Q, K, V, O (bf16) and LSE (fp32), each 256-byte aligned.
+ * Returns 0 for an invalid shape.
+ */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_fwd_host -- the same operation on HOST buffers: copies Q, K, V from
+ * host to the device workspace, runs fa_fwd, and copies O and LSE back, all
+ * enqueued on `stream` (asynchronous; synchronise the stream before reading
+ * O_host / LSE_host).  Host buffers should be pinned for the copies to
+ * overlap; pageable memory works but the copies then block the host.
+ *
+ *   Q_host, K_host, V_host  bf16 [B, H, N, d] in host memory (read).
+ *   O_host                  bf16 [B, H, N, d] in host memory (written).
+ *   LSE_host                fp32 [B, H, N] in host memory (written).
+ *   workspace               caller-owned device memory of at least
+ *                           fa_fwd_host_workspace_bytes(B, H, N, d) bytes,
+ *                           256-byte aligned; contents are scratch.
+ * Other arguments and errors as fa_fwd; FA_ERR_WORKSPACE if the workspace
+ * is NULL, too small or misaligned.
+ */
+int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host,
+                void *O_host, float *LSE_host, void *workspace,
+                size_t workspace_bytes, int B, int H, int N, int d,
+                int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_device_error -- synchronises `stream`, then reads and clears the
+ * library's device status word on the current device.  Returns FA_OK, or
+ * FA_ERR_TIMEOUT if a kernel since the last call gave up on a bounded wait
+ * (every wait inside the kernels has a time limit; on expiry the kernel
+ * drains its own copies, frees its tensor memory and exits early, leaving
+ * its outputs undefined), or FA_ERR_LAUNCH if the synchronisation itself
+ * reported a CUDA error.
+ */
+int fa_device_error(fa_stream_t stream);
+
+/*
+ * fa_selftest_bounded_wait -- runs a one-CTA kernel that waits on a barrier
+ * nothing ever signals, with the same bounded-wait code the forward kernel
+ * uses and a limit of `limit_us` microseconds (1 .. 1000000).  It checks
+ * that an expired wait ends the kernel with a status instead of a hang.
+ * Returns the device status the kernel left (FA_ERR_TIMEOUT when the
+ * mechanism works), after synchronising `stream`.  The status word is
+ * cleared before returning.
+ */
+int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char *fa_status_string(int status);
+
+/* Text of the last CUDA failure seen by this thread inside the library
+ * (the failing call and CUDA's error name), or "" if none.  The buffer is
+ * thread-local and stays valid until this thread's next failing call. */
+const char *fa_last_error_detail(void);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

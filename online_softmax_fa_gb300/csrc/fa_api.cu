@@ -1,0 +1,225 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, the
+// device-architecture check, TMA tensor-map encoding, and the host-buffer
+// wrapper.  Every check runs on the host before the first CUDA call, so a
+// rejected request enqueues nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cstdio>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per in-kernel wait
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+int check_arch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_ARCH;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
+    int state = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (state == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess)
+            return FA_ERR_ARCH;
+        state = (major == 10 && minor == 3) ? 1 : -1;
+        g_arch_ok[dev].store(state, std::memory_order_relaxed);
+    }
+    return state == 1 ? FA_OK : FA_ERR_ARCH;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost).  Box = 64 columns
+// (128 bytes, the 128-byte swizzle span) x 128 rows x 1 head.  Rows past N
+// inside a head read as zero, so a ragged tail never touches the next head.
+bool encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Shape and scalar checks shared by both entry points.
+int check_shape(int B, int H, int N, int d, float scale) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+    if (static_cast<long long>(B) * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
+    const long long qblocks = (static_cast<long long>(N) + 255) / 256;
+    if (qblocks * B * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;  // grid size
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_SCALE;
+    return FA_OK;
+}
+
+thread_local char g_detail[256] = "";
+
+}  // namespace
+
+namespace fa {
+int record_cuda_error(cudaError_t e, const char *what) {
+    std::snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return FA_ERR_LAUNCH;
+}
+int record_message(int status, const char *what) {
+    std::snprintf(g_detail, sizeof g_detail, "%s", what);
+    return status;
+}
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+           int N, int d, int causal, float scale, fa_stream_t stream) {
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
+    int rc = check_shape(B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (mis16(Q) || mis16(K) || mis16(V) || mis16(O) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+        return FA_ERR_ALIGN;
+    const size_t n_elem = static_cast<size_t>(B) * H * N * d;
+    const size_t t_bytes = n_elem * 2, l_bytes = static_cast<size_t>(B) * H * N * 4;
+    for (const void *in : {Q, K, V})
+        if (overlaps(O, t_bytes, in, t_bytes) || overlaps(LSE, l_bytes, in, t_bytes))
+            return FA_ERR_ALIAS;
+    if (overlaps(O, t_bytes, LSE, l_bytes)) return FA_ERR_ALIAS;
+
+    rc = check_arch();
+    if (rc != FA_OK) return rc;
+    CUtensorMap tmQ, tmK, tmV;
+    const int BH = B * H;
+    if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, BH, N, d) ||
+        !encode_qkv_map(&tmV, V, BH, N, d))
+        return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    fa::LaunchArgs a;
+    a.tmQ = &tmQ;
+    a.tmK = &tmK;
+    a.tmV = &tmV;
+    a.O = O;
+    a.LSE = LSE;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.causal = causal != 0;
+    a.scale = scale;
+    a.limit_ns = kWaitLimitNs;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return fa::launch_fwd(a);
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
+    const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
+    return 4 * align256(t_bytes) + align256(l_bytes);
+}
+
+int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
+                float *LSE_host, void *workspace, size_t workspace_bytes, int B, int H, int N,
+                int d, int causal, float scale, fa_stream_t stream) {
+    if (!Q_host || !K_host || !V_host || !O_host || !LSE_host) return FA_ERR_NULL;
+    int rc = check_shape(B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_WORKSPACE;
+    rc = check_arch();
+    if (rc != FA_OK) return rc;
+    const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    uint8_t *dQ = w, *dK = dQ + align256(t_bytes), *dV = dK + align256(t_bytes);
+    uint8_t *dO = dV + align256(t_bytes);
+    float *dL = reinterpret_cast<float *>(dO + align256(t_bytes));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    FA_CUDA_TRY(cudaMemcpyAsync(dQ, Q_host, t_bytes, cudaMemcpyHostToDevice, s));
+    FA_CUDA_TRY(cudaMemcpyAsync(dK, K_host, t_bytes, cudaMemcpyHostToDevice, s));
+    FA_CUDA_TRY(cudaMemcpyAsync(dV, V_host, t_bytes, cudaMemcpyHostToDevice, s));
+    rc = fa_fwd(dQ, dK, dV, dO, dL, B, H, N, d, causal, scale, stream);
+    if (rc != FA_OK) return rc;
+    FA_CUDA_TRY(cudaMemcpyAsync(O_host, dO, t_bytes, cudaMemcpyDeviceToHost, s));
+    FA_CUDA_TRY(cudaMemcpyAsync(LSE_host, dL, l_bytes, cudaMemcpyDeviceToHost, s));
+    return FA_OK;
+}
+
+int fa_device_error(fa_stream_t stream) {
+    int v = 0;
+    const int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
+    if (rc != FA_OK) return rc;
+    return v == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return FA_ERR_SHAPE;
+    int rc = check_arch();
+    if (rc != FA_OK) return rc;
+    rc = fa::launch_wait_selftest(static_cast<uint64_t>(limit_us) * 1000ull,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    if (rc != FA_OK) return rc;
+    return fa_device_error(stream);
+}
+
+const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and fit the indexing)";
+        case FA_ERR_HEADDIM: return "head dimension d must be 64 or 128";
+        case FA_ERR_ALIGN: return "Q, K, V, O must be 16-byte aligned and LSE 4-byte aligned";
+        case FA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
+        case FA_ERR_LAUNCH: return "a CUDA call failed";
+        case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+        case FA_ERR_UNSUPPORTED: return "request not supported by this build";
+        case FA_ERR_SCALE: return "scale must be a finite number > 0";
+        case FA_ERR_ALIAS: return "an output buffer overlaps an input buffer";
+        case FA_ERR_WORKSPACE: return "workspace NULL, too small or not 256-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+int fa_version(void) { return 100; }
+
+const char *fa_last_error_detail(void) { return g_detail; }
+
+}  // extern "C"

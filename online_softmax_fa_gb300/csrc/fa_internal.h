@@ -1,0 +1,39 @@
+// fa_internal.h -- declarations shared by the C-ABI layer (fa_api.cu) and the
+// kernel translation unit (fa_fwd_sm103.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+struct LaunchArgs {
+    const CUtensorMap *tmQ, *tmK, *tmV;
+    void *O;
+    float *LSE;
+    int BH, N, d;
+    bool causal;
+    float scale;
+    uint64_t limit_ns;  // bound on every in-kernel wait
+    cudaStream_t stream;
+};
+
+int launch_fwd(const LaunchArgs &a);
+
+// Records the CUDA error of a failed call (thread-local) for
+// fa_last_error_detail(); returns FA_ERR_LAUNCH.
+int record_cuda_error(cudaError_t e, const char *what);
+int record_message(int status, const char *what);
+#define FA_CUDA_TRY(call)                                              \
+    do {                                                               \
+        cudaError_t fa_e_ = (call);                                    \
+        if (fa_e_ != cudaSuccess) return ::fa::record_cuda_error(fa_e_, #call); \
+    } while (0)
+int read_and_clear_status(cudaStream_t stream, int *status);
+int launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fa

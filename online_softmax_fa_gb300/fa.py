@@ -1,0 +1,140 @@
+"""ctypes binding of the C ABI in ``include/fa.h`` -- argument marshalling only.
+
+Every step of the attention forward pass runs in the CUDA library
+``_build/libfa_gb300.so``; this module passes pointers, sizes and the
+current torch stream.  There is no fallback: if the library is missing or a
+call fails, it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_TIMEOUT = -7
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = load_library().fa_last_error_detail().decode()
+        super().__init__(f"{where}: {fa_status_string(status)} (status {status})"
+                         + (f" [{detail}]" if detail else ""))
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load (once) the in-tree CUDA library; raise if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
+    lib.fa_fwd.restype = I
+    lib.fa_fwd_host_workspace_bytes.argtypes = [I, I, I, I]
+    lib.fa_fwd_host_workspace_bytes.restype = S
+    lib.fa_fwd_host.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
+    lib.fa_fwd_host.restype = I
+    lib.fa_device_error.argtypes = [P]
+    lib.fa_device_error.restype = I
+    lib.fa_selftest_bounded_wait.argtypes = [I, P]
+    lib.fa_selftest_bounded_wait.restype = I
+    lib.fa_status_string.argtypes = [I]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_error_detail.argtypes = []
+    lib.fa_last_error_detail.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = I
+    _lib = lib
+    return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, d]")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return tuple(int(x) for x in q.shape)
+
+
+def fa_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+           stream=None):
+    """O = softmax(scale * q k^T [+causal]) v and LSE, on the current stream.
+
+    q, k, v: contiguous CUDA bf16 [B, H, N, d].  o (bf16 [B,H,N,d]) and lse
+    (fp32 [B,H,N]) are allocated when not given.  Returns (o, lse).
+    """
+    import torch
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, 1 if causal else 0,
+                               float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, workspace,
+                causal: bool = False, scale: float | None = None, stream=None):
+    """Host-buffer variant: H2D copies, the kernel and D2H copies, all
+    enqueued on one stream.  Tensors are CPU (ideally pinned); ``workspace``
+    is a CUDA uint8 tensor of at least fa_fwd_host_workspace_bytes bytes.
+    Asynchronous: synchronise the stream before reading o_host/lse_host."""
+    B, H, N, d = (int(x) for x in q_host.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load_library().fa_fwd_host(
+        q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+        lse_host.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host")
+
+
+def fa_device_error(stream=None) -> int:
+    return int(load_library().fa_device_error(_stream_handle(stream)))
+
+
+def fa_selftest_bounded_wait(limit_us: int, stream=None) -> int:
+    return int(load_library().fa_selftest_bounded_wait(int(limit_us), _stream_handle(stream)))
+
+
+def fa_version() -> int:
+    return int(load_library().fa_version())

@@ -1,0 +1,119 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from online_softmax_fa_gb300.build import build_library
+    from online_softmax_fa_gb300 import fa
+    build_library()
+    return fa.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("fa_fwd", "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_device_error",
+                 "fa_status_string", "fa_selftest_bounded_wait", "fa_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from online_softmax_fa_gb300 import fa
+    for code in range(0, -12, -1):
+        s = fa.fa_status_string(code)
+        assert s and s != "unknown status"
+    assert fa.fa_status_string(-999) == "unknown status"
+    assert fa.fa_version() >= 100
+
+
+def _call(lib, Q=16, K=32, V=48, O=4096, L=8192, B=1, H=1, N=8, d=64, causal=0,
+          scale=0.125):
+    return lib.fa_fwd(Q, K, V, O, L, B, H, N, d, causal, scale, None)
+
+
+# Fake, never-dereferenced addresses: the checks below must reject each
+# request on the host before any pointer is touched.
+def test_null_pointers(lib):
+    assert _call(lib, Q=None) == -1
+    assert _call(lib, L=None) == -1
+
+
+def test_bad_shapes(lib):
+    assert _call(lib, B=0) == -2
+    assert _call(lib, N=0) == -2
+    assert _call(lib, H=-1) == -2
+    assert _call(lib, B=1 << 16, H=1 << 16) == -2
+    assert _call(lib, d=96) == -3
+    assert _call(lib, d=256) == -3
+
+
+def test_bad_scale(lib):
+    assert _call(lib, scale=0.0) == -9
+    assert _call(lib, scale=-1.0) == -9
+    assert _call(lib, scale=float("inf")) == -9
+    assert _call(lib, scale=float("nan")) == -9
+
+
+def test_alignment(lib):
+    assert _call(lib, Q=17) == -4
+    assert _call(lib, O=4104) == -4
+    assert _call(lib, L=8194) == -4
+
+
+def test_aliasing(lib):
+    # [1,1,8,64] bf16 = 1024 bytes per tensor
+    assert _call(lib, Q=1 << 20, O=(1 << 20) + 512) == -10
+    assert _call(lib, V=1 << 20, L=(1 << 20) + 1020) == -10
+    assert _call(lib, O=1 << 20, L=(1 << 20) + 4) == -10
+
+
+def test_host_variant_checks(lib):
+    need = lib.fa_fwd_host_workspace_bytes(1, 2, 300, 64)
+    assert need >= 4 * 2 * 300 * 64 * 2 + 2 * 300 * 4
+    assert need % 256 == 0
+    assert lib.fa_fwd_host_workspace_bytes(1, 1, 8, 96) == 0
+    args = (16, 32, 48, 64, 80)
+    assert lib.fa_fwd_host(*args, None, need, 1, 2, 300, 64, 0, 0.1, None) == -11
+    assert lib.fa_fwd_host(*args, 1 << 20, need - 1, 1, 2, 300, 64, 0, 0.1, None) == -11
+    assert lib.fa_fwd_host(*args, (1 << 20) + 16, need, 1, 2, 300, 64, 0, 0.1, None) == -11
+    assert lib.fa_fwd_host(None, 32, 48, 64, 80, 1 << 20, need, 1, 2, 300, 64, 0, 0.1,
+                           None) == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_request_without_gpu_reports_arch(lib):
+    # valid arguments, but no sm_103 device: nothing may be enqueued
+    assert _call(lib, Q=1 << 20, K=2 << 20, V=3 << 20, O=4 << 20, L=5 << 20) == -5
+    assert lib.fa_selftest_bounded_wait(1000, None) == -5
+    assert lib.fa_selftest_bounded_wait(0, None) == -2
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from online_softmax_fa_gb300 import fa
+    saved = fa._lib
+    try:
+        fa._lib = None
+        with pytest.raises(RuntimeError, match="not found"):
+            fa.load_library(str(tmp_path / "missing.so"))
+    finally:
+        fa._lib = saved

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerance (bf16 output, fp32 accumulation): O max-abs <= 2e-2 and mean-abs
+<= 2e-3, LSE abs <= 1e-3, compared element by element on the same seeded
+inputs.  Small shapes are compared in full; the full-size workloads on
+sampled query rows (the oracle computes them one by one) plus properties
+that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_fa_gb300.inputs import WORKLOADS, make_qkv, make_workload, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from online_softmax_fa_gb300 import fa as fa_mod
+    from online_softmax_fa_gb300.build import build_library
+    build_library()
+    fa_mod.load_library()
+    return fa_mod
+
+
+def run(fa, q, k, v, causal, scale):
+    dev = torch.device("cuda")
+    o, lse = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check(o, lse, O_ref, L_ref, what=""):
+    eo = np.abs(o - O_ref)
+    el = np.abs(lse - L_ref)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), what
+    assert eo.max() <= O_MAX, f"{what}: O max-abs {eo.max():.3e}"
+    assert eo.mean() <= O_MEAN, f"{what}: O mean-abs {eo.mean():.3e}"
+    assert el.max() <= LSE_MAX, f"{what}: LSE max-abs {el.max():.3e}"
+    return eo.max(), eo.mean(), el.max()
+
+
+def scale_of(d):
+    return float(np.float32(1 / np.sqrt(d)))
+
+
+# --------------------------------------------------------- small, in full
+def test_tiny_workload(fa):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_workload(w)
+    o, lse = run(fa, q, k, v, False, w.scale)
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=False, scale=w.scale)
+    check(o, lse, O_ref, L_ref, "tiny")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_late_max_workload(fa, causal):
+    w = WORKLOADS["late"]
+    q, k, v = make_workload(w)
+    o, lse = run(fa, q, k, v, causal, w.scale)
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=w.scale)
+    check(o, lse, O_ref, L_ref, f"late causal={causal}")
+
+
+EDGE_N = [1, 2, 63, 127, 128, 129, 255, 256, 257, 300, 383, 512, 640, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_edge_sweep(fa, N, d, causal):
+    """Single tile, tile edges, ragged tails, odd block counts."""
+    q, k, v = make_qkv(1, 2, N, d, seed=1000 + N + d)
+    o, lse = run(fa, q, k, v, causal, scale_of(d))
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale_of(d))
+    check(o, lse, O_ref, L_ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.5, 1.0])
+def test_scales_and_large_scores(fa, scale):
+    """Scores up to ~|40|: the running max moves by large steps."""
+    q, k, v = make_qkv(2, 3, 700, 64, seed=77)
+    q = (q.float() * 2).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = run(fa, q, k, v, causal, scale)
+        O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale)
+        check(o, lse, O_ref, L_ref, f"scale={scale} causal={causal}")
+
+
+def test_batch_and_heads_layout(fa):
+    """B > 1 and H > 1 with a ragged N: heads must not bleed into each other."""
+    q, k, v = make_qkv(3, 5, 333, 128, seed=9)
+    for causal in (False, True):
+        o, lse = run(fa, q, k, v, causal, scale_of(128))
+        O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale_of(128))
+        check(o, lse, O_ref, L_ref, f"layout causal={causal}")
+
+
+# ------------------------------------------------------------ closed forms
+def test_closed_forms(fa):
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(3)
+    # identical keys -> mean of V, LSE = s + log N
+    N, d = 520, 128
+    q = torch.randn(1, 2, N, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 2, 1, d, generator=g).to(torch.bfloat16).expand(1, 2, N, d).contiguous()
+    v = torch.randn(1, 2, N, d, generator=g).to(torch.bfloat16)
+    o, lse = run(fa, q, k, v, False, 0.1)
+    mean_v = v.double().mean(dim=2, keepdim=True).numpy()
+    assert np.abs(o - mean_v).max() <= O_MAX
+    s = 0.1 * np.einsum("bhnd,bhd->bhn", q.double().numpy(), k[:, :, 0].double().numpy())
+    assert np.abs(lse - (s + np.log(N))).max() <= LSE_MAX
+    # N = 1: O = V, LSE = scale q.k
+    q1, k1, v1 = make_qkv(2, 3, 1, 64, seed=4)
+    o, lse = run(fa, q1, k1, v1, True, 0.125)
+    assert np.array_equal(o, v1.float().numpy())
+    s = 0.125 * (q1.double() * k1.double()).sum(-1).numpy()
+    assert np.abs(lse - s).max() <= LSE_MAX
+    # causal row 0 returns V_0 exactly (one key, weight 1)
+    q2, k2, v2 = make_qkv(1, 4, 700, 128, seed=5)
+    o, _ = run(fa, q2, k2, v2, True, scale_of(128))
+    assert np.array_equal(o[:, :, 0], v2[:, :, 0].float().numpy())
+
+
+def test_determinism(fa):
+    q, k, v = make_workload(WORKLOADS["late"])
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    for causal in (False, True):
+        o1, l1 = fa.fa_fwd(q, k, v, causal=causal)
+        o2, l2 = fa.fa_fwd(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# --------------------------------------------------- full-size workloads
+def _sampled_check(fa, w, rows_per_head, causal):
+    q, k, v = make_workload(w)
+    dev = torch.device("cuda")
+    o_d, lse_d = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    BH = w.B * w.H
+    # properties at full size: finite everywhere, LSE >= the row's own score
+    assert torch.isfinite(lse_d).all()
+    assert torch.isfinite(o_d.float()).all()
+    rows = sample_rows(w.N, BH, rows_per_head, seed=w.seed)
+    o = o_d.float().reshape(BH, w.N, w.d).cpu().numpy()
+    lse = lse_d.reshape(BH, w.N).cpu().numpy()
+    idx = np.arange(BH)[:, None]
+    O_ref, L_ref = oracle.attention_fwd(q.reshape(BH, w.N, w.d), k.reshape(BH, w.N, w.d),
+                                        v.reshape(BH, w.N, w.d), causal=causal,
+                                        scale=w.scale, rows=rows)
+    return check(o[idx, rows], lse[idx, rows], O_ref, L_ref, w.name)
+
+
+def test_llama_workload_sampled(fa):
+    _sampled_check(fa, WORKLOADS["llama"], 48, True)
+
+
+def test_batch_workload_sampled(fa):
+    _sampled_check(fa, WORKLOADS["batch"], 12, False)
+
+
+def test_long_ragged_workload_sampled(fa):
+    w = WORKLOADS["long"]
+    _sampled_check(fa, w, w.sampled_rows, True)
+
+
+# --------------------------------------------- host-buffer entry point
+def test_host_buffer_variant_matches(fa):
+    q, k, v = make_qkv(2, 3, 300, 128, seed=21)
+    B, H, N, d = q.shape
+    dev = torch.device("cuda")
+    need = fa.fa_fwd_host_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    for causal in (False, True):
+        fa.fa_fwd_host(qh, kh, vh, oh, lh, ws, causal=causal)
+        torch.cuda.synchronize()
+        o_d, l_d = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, o_d.cpu()) and torch.equal(lh, l_d.cpu())
+
+
+# ------------------------------------------------------ failure detection
+def test_bounded_wait_expires_with_status(fa):
+    """A wait nothing signals ends with FA_ERR_TIMEOUT, not a hang, and the
+    context stays usable afterwards."""
+    assert fa.fa_selftest_bounded_wait(20000) == fa.FA_ERR_TIMEOUT
+    assert fa.fa_device_error() == 0  # the status word was cleared
+    q, k, v = make_qkv(1, 1, 256, 64, seed=1)
+    o, lse = run(fa, q, k, v, False, 0.125)
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, scale=0.125)
+    check(o, lse, O_ref, L_ref, "after selftest")
