@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward TFLOP/s on GB300 (one JSON line).
+
+Workload (default): the Llama-3-8B layer shape B=1, H=32, N=8192, d=128,
+causal, bf16 Q/K/V i.i.d. N(0,1) from seed 3, scale 1/sqrt(128).
+Metric: 4*B*H*N^2*d / t, halved for causal, in TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+ours: W warm-up steps, then exactly K timed steps (one fa_fwd launch each),
+  bracketed by a barrier and a device synchronise on both sides, CUDA events
+  on the launching stream, max over ranks.  Three resident input sets
+  (3 x 256 MiB incl. outputs, > the 129 MB L2) are used in rotation, so a
+  step never finds its K/V already in L2 from the step before.  Adds the
+  end-to-end number through the host-buffer C-ABI call (pinned host memory,
+  copies inside the timed region), the roofline of the kernel, SM clocks
+  sampled during the timed region, and the fp64 CPU oracle timed on a
+  bounded sample of the same workload.
+reference: the fp64 CPU oracle as it stands, on the host cores, each step a
+  bounded sample of the same workload (rank 0 only under torchrun).
+Under torchrun every rank runs the full workload on its own GPU (weak
+scaling, no data-path collective); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from online_softmax_fa_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = ("attn fwd TFLOP/s (4·B·H·N²·d, causal halved) "
+          "and % of GB300 BF16 tensor peak")
+NOMINAL_BF16_TFLOPS = 2250.0
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_SOURCES = ["online_softmax_fa_gb300/csrc/fa_fwd_sm103.cu",
+                  "online_softmax_fa_gb300/csrc/sm103_primitives.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_llama_traffic.json")
+
+
+def workload_config(w, causal):
+    return {"workload": f"llama-3-8b-layer attention forward B{w.B} H{w.H} N{w.N} d{w.d}"
+                        + (" causal" if causal else ""),
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+            "scale": "1/sqrt(d) in fp32", "inputs": f"bf16 i.i.d. N(0,1), seed {w.seed}",
+            "l2": "inputs > L2: 3 resident input sets of 256 MiB used in rotation"}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a host float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 0.0, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from an ncu capture, if taken on this kernel."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_source_digest():
+        return None  # the kernel changed since the counters were taken
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def row_flops(rows: np.ndarray, N: int, d: int, causal: bool) -> float:
+    """Nominal FLOPs of the given query rows (4*d per attended key)."""
+    if causal:
+        return float(4.0 * d * np.sum(rows.astype(np.float64) + 1.0))
+    return float(4.0 * d * N * rows.size)
+
+
+def oracle_sample(w, causal, q, k, v, rows_per_head, nthreads, offset=0):
+    """Time the fp64 oracle on `rows_per_head` evenly spread rows of every
+    head; returns (seconds, nominal FLOPs of those rows)."""
+    import oracle
+    BH = w.B * w.H
+    stride = max(1, w.N // rows_per_head)
+    base = (np.arange(rows_per_head, dtype=np.int64) * stride + offset) % w.N
+    rows = np.broadcast_to(base, (BH, rows_per_head)).copy()
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, causal=causal, scale=w.scale, rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, row_flops(rows, w.N, w.d, causal)
+
+
+def oracle_inputs(w):
+    import oracle
+    q, k, v = make_workload(w)
+    BH = w.B * w.H
+    shp = (BH, w.N, w.d)
+    return tuple(oracle.bf16_bits_to_f64(t.reshape(shp)) for t in (q, k, v))
+
+
+def cpu_baseline(w, causal, target_s=15.0):
+    import oracle
+    qf, kf, vf = oracle_inputs(w)
+    nth = oracle.default_threads()
+    dt, _ = oracle_sample(w, causal, qf, kf, vf, 8, nth)  # calibration
+    per_row = dt / 8
+    rph = int(min(w.N, max(8, target_s / max(per_row, 1e-6))))
+    dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+            "sample": f"{rph} evenly spaced query rows in each of the {w.B * w.H} heads "
+                      f"({rph * w.B * w.H} rows, {dt:.1f} s); fp64, S and P materialised "
+                      f"over all N keys per row; FLOPs counted as 4*d per attended key"}
+
+
+def run_reference(args, w, causal):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    qf, kf, vf = oracle_inputs(w)
+    nth = oracle.default_threads()
+    dt, _ = oracle_sample(w, causal, qf, kf, vf, 8, nth)
+    per_row = dt / 8
+    budget_s = 120.0
+    total_steps = max(1, args.steps + args.warmup)
+    rph = int(min(w.N, max(1, budget_s / total_steps / max(per_row, 1e-6))))
+    for i in range(args.warmup):
+        oracle_sample(w, causal, qf, kf, vf, rph, nth, offset=i)
+    tot_t, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth, offset=args.warmup + i)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: {rph} evenly spaced query rows (offset by the step index) in each "
+              f"of the {w.B * w.H} heads; fp64 oracle, S and P materialised")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(w, causal),
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w, causal):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from online_softmax_fa_gb300 import fa
+    from online_softmax_fa_gb300.build import build_library
+    build_library()  # no-op when up to date; raises if nvcc fails
+    fa.load_library()
+
+    q, k, v = make_workload(w)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    sets = []
+    for _ in range(3):
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev),
+                     torch.empty((B, H, N), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.current_stream()
+    flops = w.flops(causal)
+
+    for i in range(args.warmup):
+        qd, kd, vd, od, ld = sets[i % 3]
+        fa.fa_fwd(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_uuid = None
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        gpu_uuid = s if s.startswith("GPU-") else "GPU-" + s
+    sampler = ClockSampler(gpu_uuid)
+    time.sleep(0.5)  # let the sampler start
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        qd, kd, vd, od, ld = sets[i % 3]
+        starts[i].record(stream)
+        fa.fa_fwd(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    status = fa.fa_device_error()
+    if status != 0:
+        raise RuntimeError(f"device status {status} during the timed region")
+    total_ms = e0.elapsed_time(e1)
+    kern_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    total_ms_max = max_over_ranks(total_ms, ws)
+    value = ws * flops * args.steps / (total_ms_max * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point: H2D of Q, K, V from
+    # pinned memory, the kernel, D2H of O and LSE -- every step
+    e2e_steps = max(3, min(args.steps, 30))
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    wsp = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                      device=dev)
+    for _ in range(2):
+        fa.fa_fwd_host(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    barrier(ws)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        fa.fa_fwd_host(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    if fa.fa_device_error() != 0:
+        raise RuntimeError("device status set during the end-to-end leg")
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1), ws)
+    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    tbytes = q.numel() * 2
+    h2d = 3 * tbytes
+    d2h = tbytes + B * H * N * 4
+
+    if rank != 0:
+        return
+    peak, peak_sust, peak_kind = load_peaks()
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w, causal),
+        "pct_of_nominal_bf16_peak": 100.0 * value / ws / NOMINAL_BF16_TFLOPS,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}",
+                     "traffic": recorded_traffic(),
+                     "kernel": f"fa_fwd_kernel<{d},{str(causal).lower()}>",
+                     "kernel_ms": kern_ms},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e2e_ms / e2e_steps,
+                "api": "fa_fwd_host (C ABI, pinned host buffers)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, causal)
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama")
+    ap.add_argument("--causal", choices=["auto", "0", "1"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    w = WORKLOADS[args.workload]
+    causal = w.causal[-1] if args.causal == "auto" else args.causal == "1"
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, causal)
+        else:
+            run_ours(args, w, causal)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
