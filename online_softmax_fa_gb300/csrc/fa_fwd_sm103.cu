@@ -10,24 +10,33 @@
 // o = a / l once at the end ("Fix 1" of "FlashAttention-2 -- Deeper Math",
 // aicassindra.com) and L = m + log(l) is written beside it ("Fix 2").
 //
-// GB300 mapping (one CTA per (b, h, 256-row query block), "Fix 3"/"Fix 4"):
-//   * warp 9 (TMA): loads the query block once, then streams 128-key K and
-//     V tiles through separate multi-stage shared-memory rings.
-//   * warp 8 (MMA): one thread issues tcgen05 MMAs.  The query block is two
-//     128-row sub-tiles; S_k = Q_k K_j^T lands in TMEM (fp32), and
-//     O_k += P_k V_j reads P_k from TMEM (bf16, written over S_k) and V_j
-//     from shared memory, accumulating O_k in TMEM.  The issue order
-//     S_0(j), PV_1(j-1), S_1(j), PV_0(j) keeps the tensor pipe busy while
-//     the two softmax groups work on the other sub-tile.
+// GB300 mapping.  A work item is one (b, h, 256-row query block): query
+// blocks are the outer loop and own their output ("Fix 3"), and the grid
+// covers batch x heads x query blocks ("Fix 4").  The kernel is persistent:
+// one CTA per SM walks a static schedule of work items, heaviest first
+// (causal blocks differ in cost), assigned in a snake order over the CTAs
+// so the per-CTA totals balance ("the assignment of blocks to SMs must
+// account for the imbalance").  Consecutive items overlap: the next item's
+// query block loads and its first S tiles are computed while the softmax
+// warps write the previous item's output.
+//   * warp 9 (TMA): per item, the query block once, then 128-key K and V
+//     tiles through separate multi-stage shared-memory rings that run on
+//     across items.
+//   * warp 8 (MMA): tcgen05 MMAs issued by one elected lane of a converged
+//     warp.  The query block is two 128-row sub-tiles; S_k = Q_k K_j^T lands
+//     in TMEM (fp32), and O_k += P_k V_j reads P_k from TMEM (bf16, written
+//     over S_k) and V_j from shared memory, accumulating O_k in TMEM.  Issue
+//     order S_0(j), PV_1(j-1), S_1(j), PV_0(j) keeps the tensor pipe busy
+//     while the two softmax groups work on the other sub-tile.
 //   * warps 0-3 / 4-7 (softmax, one group per sub-tile; thread = row):
 //     TMEM -> registers, mask (diagonal / ragged tiles only), row max with
 //     the scale folded into base-2 exponents, p = 2^(s*c - m), row sum in
 //     fp32, P -> TMEM as bf16, and the rescale of O_k in TMEM only for
-//     warps where some row's max moved.  After the last tile: O = a / l in
-//     bf16 and LSE = (m + log2 l) ln 2.
+//     warps where some row's reference max moved.  After an item's last
+//     tile: O = a / l in bf16 and LSE = (m + log2 l) ln 2.
 //   * causal: key tiles entirely above the diagonal are never loaded or
 //     computed; only diagonal tiles are masked ("Causal masking: skip the
-//     blocks, do not mask them"), and CTAs start heaviest query block first.
+//     blocks, do not mask them").
 //
 // TMEM columns (512 allocated): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_k occupies the first 64 columns
@@ -47,19 +56,28 @@ namespace fa {
 // bounded wait that expired.
 __device__ int g_fa_status;
 
-constexpr int kBlockM = 256;  // query rows per CTA (two 128-row sub-tiles)
+constexpr int kBlockM = 256;  // query rows per work item (two 128-row sub-tiles)
 constexpr int kSubM = 128;    // rows per sub-tile = TMEM lanes
 constexpr int kBlockN = 128;  // keys per K/V tile
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
-constexpr int kThreads = 320;         // 10 warps
+constexpr int kThreads = 384;         // 12 warps = 3 warpgroups
 constexpr int kMmaWarp = 8;
-constexpr int kTmaWarp = 9;
+constexpr int kTmaWarp = 9;           // warps 10, 11: no role (warpgroup padding)
+// Registers per thread after reallocation.  Launch: 384 threads x 168.
+// Warpgroup 2 (MMA, TMA) gives back down to 72; the two softmax warpgroups
+// take 216 each: 128 x (216 + 216 + 72) = 64512 = 384 x 168, and each SM
+// sub-partition holds one warp of each: 32 x 504 <= 16384 registers.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kTmemCols = 512;
+// The running reference max moves only when a row's max exceeds it by more
+// than this many base-2 units (factor 256); probabilities then stay <= 256.
+constexpr float kStaleMax = 8.0f;
 
 // wait sites recorded in the status word on a timeout
 enum : int {
     kSiteQ = 1, kSiteKFull, kSiteVFull, kSitePFull, kSiteKEmpty, kSiteVEmpty,
-    kSiteSFull, kSiteOFull
+    kSiteSFull, kSiteOFull, kSiteQEmpty, kSiteOEmpty
 };
 
 template <int D>
@@ -72,9 +90,10 @@ struct Cfg {
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
-    // s_full[2], p_full[2], o_full, then tmem slot + abort flag
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
+    // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S],
+    // v_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], mma_done;
+    // then the tmem slot and the abort flag
+    static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
@@ -84,223 +103,334 @@ struct Cfg {
     static_assert(256 + 2 * D <= (int)kTmemCols, "TMEM budget");
 };
 
+// S = Q_k K_j^T: D/16 MMAs of M128 x N128 x K16, both operands K-major in
+// 64-column swizzled chunks; K-step kk sits in chunk kk/4 at byte 32*(kk%4).
+// A descriptor's low bits hold (address >> 4), so byte offsets are added as
+// (offset >> 4).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tm, uint64_t dq, uint64_t dk) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+        mma_ss_elect(d_tm, dq + off, dk + off, Cfg<D>::kIdescS, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O_k += P_k V_j: 8 MMAs of M128 x N(D) x K16; P_k from TMEM (16 keys = 8
+// columns of packed bf16 pairs), V_j MN-major, 16 keys = 2048 bytes.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tm, uint32_t p_tm, uint64_t dv, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < kBlockN / 16; ++kk)
+        mma_ts_elect(d_tm, p_tm + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                     Cfg<D>::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+}
+
 struct Params {
     __nv_bfloat16 *O;
     float *LSE;
     int N;
+    int BH;         // batch x heads
     int n_qblocks;  // ceil(N / 256)
     int n_ktiles;   // ceil(N / 128)
+    int n_items;    // BH x n_qblocks
     float scale_log2;  // scale * log2(e)
     uint64_t limit_ns;
 };
 
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
-                  const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+// Shared-memory layout of one CTA (rebuilt where needed: it costs a few
+// integer instructions and keeps nothing live across register reallocation).
+template <int D>
+struct SmemView {
+    uint8_t *q, *k, *v;
+    uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty;
+    uint64_t *s_full, *p_full, *o_full, *o_empty, *mma_done;
+    uint32_t *tmem_slot;
+    volatile int *abort_flag;
+};
+
+template <int D>
+__device__ __forceinline__ SmemView<D> smem_view() {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem + C::kOffQ;
-    uint8_t *sK = smem + C::kOffK;
-    uint8_t *sV = smem + C::kOffV;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *q_full = bars;
-    uint64_t *k_full = bars + 1;
-    uint64_t *k_empty = k_full + C::kStages;
-    uint64_t *v_full = k_empty + C::kStages;
-    uint64_t *v_empty = v_full + C::kStages;
-    uint64_t *s_full = v_empty + C::kStages;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_full = p_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    SmemView<D> v;
+    v.q = smem + C::kOffQ;
+    v.k = smem + C::kOffK;
+    v.v = smem + C::kOffV;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    v.q_full = b;
+    v.q_empty = b + 1;
+    v.k_full = b + 2;
+    v.k_empty = v.k_full + C::kStages;
+    v.v_full = v.k_empty + C::kStages;
+    v.v_empty = v.v_full + C::kStages;
+    v.s_full = v.v_empty + C::kStages;
+    v.p_full = v.s_full + 2;
+    v.o_full = v.p_full + 2;
+    v.o_empty = v.o_full + 2;
+    v.mma_done = v.o_empty + 2;
+    v.tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    v.abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    return v;
+}
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+// ------------------------------------------------------------- schedule
+// Work items in cost order.  Causal: heaviest query block first (block qb
+// needs 2*qb + 2 key tiles), heads interleaved; otherwise head-major (equal
+// cost, and consecutive items share K/V in L2).
+struct Work {
+    int bh, qb, n_sub0, n_sub1;  // n_sub1 >= n_sub0
+};
 
-    // ---- work item: head-major, heaviest query block first when causal
-    const int bh = blockIdx.x / p.n_qblocks;
-    const int qi = blockIdx.x % p.n_qblocks;
-    const int qb = CAUSAL ? (p.n_qblocks - 1 - qi) : qi;
-    const int N = p.N;
-    const int T = p.n_ktiles;
-    // key tiles each sub-tile needs (causal: up to its last row's diagonal)
-    const int n_sub0 = CAUSAL ? min(T, min(qb * kBlockM + kSubM - 1, N - 1) / kBlockN + 1) : T;
-    const int n_sub1 =
-        CAUSAL ? min(T, min(qb * kBlockM + 2 * kSubM - 1, N - 1) / kBlockN + 1) : T;
-    const int n_tiles = n_sub1;  // n_sub1 >= n_sub0
-
-    // ---- setup
-    if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
-        }
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(&s_full[k], 1);
-            mbar_init(&p_full[k], 4);  // one arrive per softmax warp
-        }
-        mbar_init(o_full, 1);
-        *abort_flag = 0;
-        fence_mbarrier_init();
-    }
-    if (warp == kTmaWarp && lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    const WaitCtl ctl{abort_flag, &g_fa_status, p.limit_ns};
-
-    if (warp == kTmaWarp) {
-        // =========================== TMA producer ===========================
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_last();
-            int issued_k = 0, issued_v = 0;
-            mbar_arrive_expect_tx(q_full, C::kQBytes);
-            for (int k = 0; k < 2; ++k)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sQ + (k * C::kChunks + c) * kBoxBytes, &tmQ, q_full, 64 * c,
-                                qb * kBlockM + k * kSubM, bh, pol_q);
-            bool ok = true;
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1;
-                if (j >= C::kStages) ok = mbar_wait(&k_empty[s], ph ^ 1, ctl, kSiteKEmpty);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + s * C::kTileBytes + c * kBoxBytes, &tmK, &k_full[s], 64 * c,
-                                j * kBlockN, bh, pol_kv);
-                ++issued_k;
-                if (j >= C::kStages) ok = mbar_wait(&v_empty[s], ph ^ 1, ctl, kSiteVEmpty);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sV + s * C::kTileBytes + c * kBoxBytes, &tmV, &v_full[s], 64 * c,
-                                j * kBlockN, bh, pol_kv);
-                ++issued_v;
-            }
-            // Drain: every load issued must land before the CTA exits.
-            mbar_wait_drain(q_full, 0, p.limit_ns);
-            for (int t = max(0, issued_k - C::kStages); t < issued_k; ++t)
-                mbar_wait_drain(&k_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
-            for (int t = max(0, issued_v - C::kStages); t < issued_v; ++t)
-                mbar_wait_drain(&v_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
-        }
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ============================ MMA issuer ============================
-        if (lane == 0) {
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t k_base = smem_u32(sK);
-            const uint32_t v_base = smem_u32(sV);
-            auto issue_S = [&](int k, int s) {
-                const uint32_t d_tm = tmem + (k ? C::kTmS1 : C::kTmS0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(q_base + k * C::kChunks * kBoxBytes + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_base + s * C::kTileBytes + off, 16, 1024);
-                    mma_ss(d_tm, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_PV = [&](int k, int s, bool acc) {
-                const uint32_t d_tm = tmem + (k ? C::kTmO1 : C::kTmO0);
-                const uint32_t p_tm = tmem + (k ? C::kTmS1 : C::kTmS0);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(v_base + s * C::kTileBytes + kk * 16 * 128,
-                                                   kBoxBytes, 1024);
-                    mma_ts(d_tm, p_tm + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = mbar_wait(q_full, 0, ctl, kSiteQ);
-            tc_fence_after();
-            for (int j = 0; j <= n_tiles && ok; ++j) {
-                const int s = j % C::kStages;
-                if (j < n_tiles) {
-                    ok = mbar_wait(&k_full[s], (j / C::kStages) & 1, ctl, kSiteKFull);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                // S_0(j)
-                if (j < n_sub0) {
-                    issue_S(0, s);
-                    mma_commit(&s_full[0]);
-                }
-                // PV_1(j-1)
-                if (j >= 1 && j - 1 < n_sub1) {
-                    const int jp = j - 1, sp = jp % C::kStages;
-                    if (jp >= n_sub0) {  // V_{j-1} not yet waited for by PV_0
-                        ok = mbar_wait(&v_full[sp], (jp / C::kStages) & 1, ctl, kSiteVFull);
-                        if (!ok) break;
-                    }
-                    ok = mbar_wait(&p_full[1], jp & 1, ctl, kSitePFull);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_PV(1, sp, jp > 0);
-                    mma_commit(&v_empty[sp]);
-                }
-                if (j < n_tiles) {
-                    // S_1(j)
-                    if (j < n_sub1) {
-                        issue_S(1, s);
-                        mma_commit(&s_full[1]);
-                    }
-                    mma_commit(&k_empty[s]);
-                    // PV_0(j)
-                    if (j < n_sub0) {
-                        ok = mbar_wait(&v_full[s], (j / C::kStages) & 1, ctl, kSiteVFull);
-                        if (!ok) break;
-                        ok = mbar_wait(&p_full[0], j & 1, ctl, kSitePFull);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_PV(0, s, j > 0);
-                    }
-                }
-            }
-            // All MMAs (or, after an abort, all issued ones) complete before
-            // o_full fires; the drain below makes the exit safe either way.
-            mma_commit(o_full);
-            mbar_wait_drain(o_full, 0, p.limit_ns);
-        }
-        __syncwarp();
+template <bool CAUSAL>
+__device__ __forceinline__ Work work_of(const Params &p, int x) {
+    Work w;
+    if (CAUSAL) {
+        w.qb = p.n_qblocks - 1 - x / p.BH;
+        w.bh = x % p.BH;
     } else {
-        // ======================= softmax (sub-tile k) =======================
-        const int k = warp >> 2;  // warps 0-3 -> 0, 4-7 -> 1
-        const int wq = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = wq * 32 + lane;
-        const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tm_s = tmem + lane_bits + (k ? C::kTmS1 : C::kTmS0);
-        const uint32_t tm_o = tmem + lane_bits + (k ? C::kTmO1 : C::kTmO0);
-        const int sub_start = qb * kBlockM + k * kSubM;
-        const int qrow = sub_start + row;
-        const float cs = p.scale_log2;
-        const int n_k = k ? n_sub1 : n_sub0;
+        w.bh = x / p.n_qblocks;
+        w.qb = x % p.n_qblocks;
+    }
+    const int T = p.n_ktiles, N = p.N;
+    // key tiles each 128-row sub-tile needs (causal: up to its last row)
+    w.n_sub0 = CAUSAL ? min(T, min(w.qb * kBlockM + kSubM - 1, N - 1) / kBlockN + 1) : T;
+    w.n_sub1 = CAUSAL ? min(T, min(w.qb * kBlockM + 2 * kSubM - 1, N - 1) / kBlockN + 1) : T;
+    return w;
+}
 
-        float m = -INFINITY;  // running max of s * scale * log2(e)
-        float l = 0.f;        // running sum of 2^(s*c - m)
-        bool ok = true;
-        for (int j = 0; j < n_k; ++j) {
-            ok = mbar_wait(&s_full[k], j & 1, ctl, kSiteSFull);
+// The r-th work item of this CTA: rows of gridDim.x items, walked left to
+// right on even rows and right to left on odd rows (a snake), so that a CTA
+// taking a heavy item from one row takes a light one from the next.
+// Returns -1 past the end.
+__device__ __forceinline__ int item_of(int r, int n_items) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int x = r * G + ((r & 1) ? (G - 1 - c) : c);
+    return x < n_items ? x : -1;
+}
+
+// ================================ TMA producer ================================
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                                              const CUtensorMap *tmV, const Params &p,
+                                              int lane) {
+    using C = Cfg<D>;
+    if (lane != 0) return;
+    const SmemView<D> v = smem_view<D>();
+    const WaitCtl ctl{v.abort_flag, &g_fa_status, p.limit_ns};
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    int g = 0;       // K/V tiles issued so far, across items
+    int items = 0;   // query blocks issued so far
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int x = item_of(r, p.n_items);
+        if (x < 0) break;
+        const Work w = work_of<CAUSAL>(p, x);
+        if (r > 0) {  // the previous item's last S MMA has read Q
+            ok = mbar_wait(v.q_empty, (r - 1) & 1, ctl, kSiteQEmpty);
             if (!ok) break;
+        }
+        mbar_arrive_expect_tx(v.q_full, C::kQBytes);
+        for (int k = 0; k < 2; ++k)
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(v.q + (k * C::kChunks + c) * kBoxBytes, tmQ, v.q_full, 64 * c,
+                            w.qb * kBlockM + k * kSubM, w.bh, pol_q);
+        ++items;
+        for (int j = 0; j < w.n_sub1; ++j) {
+            const int t = g + j, s = t % C::kStages;
+            const uint32_t ph = (t / C::kStages) & 1;
+            if (t >= C::kStages) ok = mbar_wait(&v.k_empty[s], ph ^ 1, ctl, kSiteKEmpty);
+            if (!ok) {
+                g = t;
+                break;
+            }
+            mbar_arrive_expect_tx(&v.k_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(v.k + s * C::kTileBytes + c * kBoxBytes, tmK, &v.k_full[s], 64 * c,
+                            j * kBlockN, w.bh, pol_kv);
+            if (t >= C::kStages) ok = mbar_wait(&v.v_empty[s], ph ^ 1, ctl, kSiteVEmpty);
+            if (!ok) {  // K of tile t is in flight: count it for the drain
+                g = t + 1;
+                break;
+            }
+            mbar_arrive_expect_tx(&v.v_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(v.v + s * C::kTileBytes + c * kBoxBytes, tmV, &v.v_full[s], 64 * c,
+                            j * kBlockN, w.bh, pol_kv);
+        }
+        if (ok) g += w.n_sub1;
+    }
+    // Drain: every load issued must land before the CTA exits.  The last
+    // query block, and the last load of each ring stage (after an abort V
+    // may lag K by one tile; a wait on a phase that never started times out
+    // after the limit, a wait on one that completed returns at once).
+    if (items > 0) mbar_wait_drain(v.q_full, (items - 1) & 1, p.limit_ns);
+    for (int t = max(0, g - C::kStages); t < g; ++t) {
+        mbar_wait_drain(&v.k_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+        mbar_wait_drain(&v.v_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+    }
+}
+
+// ================================= MMA issuer =================================
+// The whole warp runs this loop (converged, operands warp-uniform); elect.sync
+// inside the issue helpers picks the issuing lane.  Every wait result is made
+// warp-uniform (__all_sync), so the warp leaves the loops together and stays
+// converged for elect.sync even when a wait gives up.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void role_mma(const Params &p) {
+    using C = Cfg<D>;
+    const SmemView<D> v = smem_view<D>();
+    const WaitCtl ctl{v.abort_flag, &g_fa_status, p.limit_ns};
+    const uint32_t tmem = *v.tmem_slot;
+    const uint64_t dq0 = sdesc_sw128(smem_u32(v.q), 16, 1024);
+    const uint64_t dq1 = dq0 + ((C::kChunks * kBoxBytes) >> 4);
+    const uint64_t dk0 = sdesc_sw128(smem_u32(v.k), 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(smem_u32(v.v), kBoxBytes, 1024);
+    const uint32_t tS0 = tmem + C::kTmS0, tS1 = tmem + C::kTmS1;
+    const uint32_t tO0 = tmem + C::kTmO0, tO1 = tmem + C::kTmO1;
+    const auto wait = [&](uint64_t *bar, uint32_t parity, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
+    };
+    int g = 0;             // K/V tiles consumed, across items
+    int pc0 = 0, pc1 = 0;  // P tiles consumed per sub-tile, across items
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int x = item_of(r, p.n_items);
+        if (x < 0) break;
+        const Work w = work_of<CAUSAL>(p, x);
+        const int n0 = w.n_sub0, n1 = w.n_sub1;
+        ok = wait(v.q_full, r & 1, kSiteQ);
+        if (!ok) break;
+        tc_fence_after();
+        for (int j = 0; j <= n1 && ok; ++j) {
+            const int t = g + j, s = t % C::kStages;
+            if (j < n1) {
+                ok = wait(&v.k_full[s], (t / C::kStages) & 1, kSiteKFull);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
+            // S_0(j)
+            if (j < n0) {
+                issue_qk<D>(tS0, dq0, dk);
+                mma_commit_elect(&v.s_full[0]);
+            }
+            // PV_1(j-1)
+            if (j >= 1) {
+                const int jp = j - 1, tp = g + jp, sp = tp % C::kStages;
+                if (jp >= n0) {  // V not yet waited for by PV_0
+                    ok = wait(&v.v_full[sp], (tp / C::kStages) & 1, kSiteVFull);
+                    if (!ok) break;
+                }
+                if (jp == 0 && r > 0) {  // O_1 read out by the previous item's epilogue
+                    ok = wait(&v.o_empty[1], (r - 1) & 1, kSiteOEmpty);
+                    if (!ok) break;
+                }
+                ok = wait(&v.p_full[1], pc1 & 1, kSitePFull);
+                if (!ok) break;
+                ++pc1;
+                tc_fence_after();
+                issue_pv<D>(tO1, tS1, dv0 + static_cast<uint64_t>((sp * C::kTileBytes) >> 4),
+                            jp > 0);
+                mma_commit_elect(&v.v_empty[sp]);
+                if (jp == n1 - 1) mma_commit_elect(&v.o_full[1]);
+            }
+            if (j < n1) {
+                // S_1(j)
+                issue_qk<D>(tS1, dq1, dk);
+                mma_commit_elect(&v.s_full[1]);
+                if (j == n1 - 1) mma_commit_elect(v.q_empty);  // last read of Q
+                mma_commit_elect(&v.k_empty[s]);
+                // PV_0(j)
+                if (j < n0) {
+                    ok = wait(&v.v_full[s], (t / C::kStages) & 1, kSiteVFull);
+                    if (!ok) break;
+                    if (j == 0 && r > 0) {
+                        ok = wait(&v.o_empty[0], (r - 1) & 1, kSiteOEmpty);
+                        if (!ok) break;
+                    }
+                    ok = wait(&v.p_full[0], pc0 & 1, kSitePFull);
+                    if (!ok) break;
+                    ++pc0;
+                    tc_fence_after();
+                    issue_pv<D>(tO0, tS0, dv0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4),
+                                j > 0);
+                    if (j == n0 - 1) mma_commit_elect(&v.o_full[0]);
+                }
+            }
+        }
+        g += n1;
+    }
+    // Every MMA issued completes before the CTA frees its tensor memory.
+    mma_commit_elect(v.mma_done);
+    mbar_wait_drain(v.mma_done, 0, p.limit_ns);
+}
+
+// ============================ softmax (sub-tile k) ============================
+// p = 2^(s*c - m) for 32 consecutive scores: packed FMA, two MUFU ex2 per
+// pair, row sum into four packed fp32 accumulators, P packed to bf16 pairs.
+__device__ __forceinline__ void exp_chunk32(const float *sv, uint64_t cs2, uint64_t neg2,
+                                            uint64_t (&rs2)[4], uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(sv[2 * t], sv[2 * t + 1]), cs2, neg2), x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        rs2[t & 3] = f2_add(rs2[t & 3], f2_pack(p0, p1));
+        pk[t] = pack_bf16x2(p0, p1);
+    }
+}
+
+__device__ __forceinline__ float sum_pairs(const uint64_t (&rs2)[4]) {
+    float a, b, c, d;
+    f2_unpack(f2_add(rs2[0], rs2[1]), a, b);
+    f2_unpack(f2_add(rs2[2], rs2[3]), c, d);
+    return (a + b) + (c + d);
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane) {
+    using C = Cfg<D>;
+    const SmemView<D> v = smem_view<D>();
+    const WaitCtl ctl{v.abort_flag, &g_fa_status, p.limit_ns};
+    const uint32_t tmem = *v.tmem_slot;
+    const int N = p.N;
+    const int k = warp >> 2;  // warps 0-3 -> sub-tile 0, 4-7 -> sub-tile 1
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tm_s = tmem + lane_bits + (k ? C::kTmS1 : C::kTmS0);
+    const uint32_t tm_o = tmem + lane_bits + (k ? C::kTmO1 : C::kTmO0);
+    uint64_t *s_full = v.s_full + k, *p_ready = v.p_full + k;
+    uint64_t *o_full = v.o_full + k, *o_empty = v.o_empty + k;
+    const float cs = p.scale_log2;
+    const uint64_t cs2 = f2_pack(cs, cs);
+
+    int sc = 0;  // S tiles consumed, across items
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int x = item_of(r, p.n_items);
+        if (x < 0) break;
+        const Work w = work_of<CAUSAL>(p, x);
+        const int sub_start = w.qb * kBlockM + k * kSubM;
+        const int qrow = sub_start + row;
+        const int n_k = k ? w.n_sub1 : w.n_sub0;
+
+        // Per row: reference max m (of s * scale * log2 e) and running sum l
+        // of 2^(s*c - m).  The reference moves only when a tile's row max
+        // exceeds it by more than kStaleMax, so p <= 2^kStaleMax; (l, O) and
+        // the final LSE use the same reference, which keeps the result exact
+        // in real arithmetic.
+        float m = -INFINITY;
+        float l = 0.f;
+        for (int j = 0; j < n_k; ++j) {
+            ok = mbar_wait(s_full, sc & 1, ctl, kSiteSFull);
+            if (!ok) break;
+            ++sc;
             tc_fence_after();
             uint32_t raw[128];
             tmem_ld128(tm_s, raw);
@@ -309,84 +439,153 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key0 = j * kBlockN;
             const bool ragged = key0 + kBlockN > N;
             const bool diag = CAUSAL && (key0 + kBlockN - 1 > sub_start);
-            if (ragged || diag) {
+            if (ragged || diag) {  // keys past N or above the diagonal -> -inf
                 int lim = N - key0;
                 if (CAUSAL) lim = min(lim, qrow - key0 + 1);
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) sv[c] = -INFINITY;
             }
-            float mx = sv[0];
+            // Row max: eight short chains of three-input max.
+            float pm[8];
 #pragma unroll
-            for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
-            const float m_new = fmaxf(m, mx * cs);
+            for (int t = 0; t < 8; ++t) pm[t] = fmax3(sv[t], sv[8 + t], sv[16 + t]);
+#pragma unroll
+            for (int c = 24; c + 16 <= kBlockN; c += 16)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) pm[t] = fmax3(pm[t], sv[c + t], sv[c + 8 + t]);
+            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
+                                   fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            const float cand = mx * cs;
+            const float m_new = (cand > m + kStaleMax) ? cand : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = (m == m_use) ? 1.f : ex2_approx(m - m_use);
-            const float neg = -m_use;
-
-            float rs0 = 0.f, rs1 = 0.f;
+            const uint64_t neg2 = f2_pack(-m_use, -m_use);
+            uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c16 = 0; c16 < kBlockN / 32; ++c16) {
+            for (int c = 0; c < kBlockN; c += 32) {
                 uint32_t pk[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float p0 = ex2_approx(fmaf(sv[32 * c16 + 2 * t], cs, neg));
-                    const float p1 = ex2_approx(fmaf(sv[32 * c16 + 2 * t + 1], cs, neg));
-                    rs0 += p0;
-                    rs1 += p1;
-                    pk[t] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tm_s + 16 * c16, pk);
+                exp_chunk32(sv + c, cs2, neg2, rs2, pk);
+                tmem_st16(tm_s + c / 2, pk);
             }
-            // rescale O_k when the max moved for some row of this warp; the
-            // S_k(j) barrier also covered PV_k(j-1), so O_k is settled
+            // Rescale O_k where the reference moved for some row of this
+            // warp; the S_k(j) barrier also covered PV_k(j-1), so O_k is
+            // settled.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tm_o + 32 * c, o);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    for (int t = 0; t < 32; t += 2) {
+                        float x0, x1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[t]), __uint_as_float(o[t + 1])),
+                                         a2), x0, x1);
+                        o[t] = __float_as_uint(x0);
+                        o[t + 1] = __float_as_uint(x1);
+                    }
                     tmem_st32(tm_o + 32 * c, o);
                 }
             }
             tmem_wait_st();
-            l = l * alpha + (rs0 + rs1);
-            m = m_new;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[k]);
+            if (lane == 0) mbar_arrive(p_ready);
+            l = l * alpha + sum_pairs(rs2);
+            m = m_new;
         }
+        if (!ok) break;
 
         // ---- epilogue: O = a / l (bf16), LSE = (m + log2 l) ln 2
-        if (ok) ok = mbar_wait(o_full, 0, ctl, kSiteOFull);
-        if (ok) {
-            tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            const bool in_range = qrow < N;
-            __nv_bfloat16 *orow = p.O + (static_cast<size_t>(bh) * N + qrow) * D;
+        ok = mbar_wait(o_full, r & 1, ctl, kSiteOFull);
+        if (!ok) break;
+        tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const bool in_range = qrow < N;
+        __nv_bfloat16 *orow = p.O + (static_cast<size_t>(w.bh) * N + qrow) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tm_o + 32 * c, o);
-                uint32_t pk[16];
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tm_o + 32 * c, o);
+            uint32_t pk[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pk[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l,
-                                        __uint_as_float(o[2 * t + 1]) * inv_l);
-                if (in_range) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-                }
-            }
+            for (int t = 0; t < 16; ++t)
+                pk[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l,
+                                    __uint_as_float(o[2 * t + 1]) * inv_l);
             if (in_range) {
-                const float lse = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-                p.LSE[static_cast<size_t>(bh) * N + qrow] = lse;
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
             }
         }
+        // O_k is read out: the next item's first PV_k may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_empty);
+        if (in_range) {
+            const float lse = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            p.LSE[static_cast<size_t>(w.bh) * N + qrow] = lse;
+        }
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using C = Cfg<D>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    {
+        const SmemView<D> v = smem_view<D>();
+        if (threadIdx.x == 0) {
+            mbar_init(v.q_full, 1);
+            mbar_init(v.q_empty, 1);
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(&v.k_full[s], 1);
+                mbar_init(&v.k_empty[s], 1);
+                mbar_init(&v.v_full[s], 1);
+                mbar_init(&v.v_empty[s], 1);
+            }
+            for (int k = 0; k < 2; ++k) {
+                mbar_init(&v.s_full[k], 1);
+                mbar_init(&v.p_full[k], 4);  // one arrive per softmax warp
+                mbar_init(&v.o_full[k], 1);
+                mbar_init(&v.o_empty[k], 4);
+            }
+            mbar_init(v.mma_done, 1);
+            *v.abort_flag = 0;
+            fence_mbarrier_init();
+        }
+        if (warp == kTmaWarp && lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        if (warp == kMmaWarp) {
+            tmem_alloc(v.tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // Each role runs inside the branch that set its register budget, and
+    // rebuilds what it needs, so no value stays live across the switch.
+    if (warp >= 8) {
+        regs_decrease<kRegsControl>();
+        if (warp == kTmaWarp)
+            role_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, p, lane);
+        else if (warp == kMmaWarp)
+            role_mma<D, CAUSAL>(p);
+        __syncwarp();
+    } else {
+        regs_increase<kRegsSoftmax>();
+        role_softmax<D, CAUSAL>(p, warp, lane);
     }
 
     // ---- teardown: every role has drained its own asynchronous work
@@ -394,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(*smem_view<D>().tmem_slot, kTmemCols);
     }
 }
 
@@ -414,30 +613,51 @@ __global__ void fa_wait_selftest_kernel(uint64_t limit_ns) {
     }
 }
 
+constexpr int kMaxDevices = 64;
+
+// SM count per device, queried once.
+static int sm_count(int dev) {
+    static int counts[kMaxDevices] = {0};
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 template <int D, bool CAUSAL>
 static int launch_t(const LaunchArgs &a) {
     using C = Cfg<D>;
     auto kern = fa_fwd_kernel<D, CAUSAL>;
-    static int configured_device = -1;  // attribute set once per process
+    static int configured[kMaxDevices] = {0};  // attribute set once per device
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
-    if (configured_device != dev) {
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
+    if (!configured[dev]) {
         FA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes));
-        configured_device = dev;
+        configured[dev] = 1;
     }
+    const int sms = sm_count(dev);
+    if (sms <= 0) return record_message(FA_ERR_LAUNCH, "cannot query the SM count");
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(a.O);
     p.LSE = a.LSE;
     p.N = a.N;
+    p.BH = a.BH;
     p.n_qblocks = (a.N + kBlockM - 1) / kBlockM;
     p.n_ktiles = (a.N + kBlockN - 1) / kBlockN;
+    const long long items = static_cast<long long>(p.n_qblocks) * a.BH;
+    if (items > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
+    p.n_items = static_cast<int>(items);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
-    const long long grid = static_cast<long long>(p.n_qblocks) * a.BH;
-    if (grid > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
-    kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK,
-                                                                             *a.tmV, p);
+    // one persistent CTA per SM (the shared-memory footprint allows one)
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, p);
     FA_CUDA_TRY(cudaGetLastError());
     return FA_OK;
 }
