@@ -78,6 +78,12 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def aggregate_tflops(flops_per_rank: float, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of `flops_per_rank`
+    (weak scaling), timed by the slowest rank (`max_ms` for all steps)."""
+    return world * flops_per_rank * steps / (max_ms * 1e-3) / 1e12
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -297,7 +303,7 @@ def run_ours(args, w, causal):
     total_ms = e0.elapsed_time(e1)
     kern_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
     total_ms_max = max_over_ranks(total_ms, ws)
-    value = ws * flops * args.steps / (total_ms_max * 1e-3) / 1e12
+    value = aggregate_tflops(flops, args.steps, total_ms_max, ws)
 
     # end to end through the host-buffer entry point: H2D of Q, K, V from
     # pinned memory, the kernel, D2H of O and LSE -- every step
@@ -321,7 +327,7 @@ def run_ours(args, w, causal):
     if fa.fa_device_error() != 0:
         raise RuntimeError("device status set during the end-to-end leg")
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), ws)
-    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = aggregate_tflops(flops, e2e_steps, e2e_ms, ws)
     tbytes = q.numel() * 2
     h2d = 3 * tbytes
     d2h = tbytes + B * H * N * 4
