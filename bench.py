@@ -50,9 +50,10 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_llama_traffic.json")
 
 
 def workload_config(w, causal):
-    return {"workload": f"llama-3-8b-layer attention forward B{w.B} H{w.H} N{w.N} d{w.d}"
+    kv = f" (K/V heads {w.kv_heads})" if w.kv_heads != w.H else ""
+    return {"workload": f"{w.name} attention forward B{w.B} H{w.H}{kv} N{w.N} d{w.d}"
                         + (" causal" if causal else ""),
-            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+            "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N, "d": w.d, "causal": causal,
             "scale": "1/sqrt(d) in fp32", "inputs": f"bf16 i.i.d. N(0,1), seed {w.seed}",
             "l2": "inputs > L2: 3 resident input sets of 256 MiB used in rotation"}
 
@@ -260,6 +261,8 @@ def run_ours(args, w, causal):
 
     q, k, v = make_workload(w)
     B, H, N, d = w.B, w.H, w.N, w.d
+    gqa = w.kv_heads != w.H
+    step = fa.fa_fwd_gqa if gqa else fa.fa_fwd
     sets = []
     for _ in range(3):
         sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev),
@@ -269,7 +272,7 @@ def run_ours(args, w, causal):
 
     for i in range(args.warmup):
         qd, kd, vd, od, ld = sets[i % 3]
-        fa.fa_fwd(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
+        step(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
     if fa.fa_device_error() != 0:
         raise RuntimeError("device status set during warm-up")
@@ -291,7 +294,7 @@ def run_ours(args, w, causal):
     for i in range(args.steps):
         qd, kd, vd, od, ld = sets[i % 3]
         starts[i].record(stream)
-        fa.fa_fwd(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
+        step(qd, kd, vd, od, ld, causal=causal, scale=w.scale)
         ends[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -306,14 +309,15 @@ def run_ours(args, w, causal):
     value = aggregate_tflops(flops, args.steps, total_ms_max, ws)
 
     # end to end through the host-buffer entry point: H2D of Q, K, V from
-    # pinned memory, the kernel, D2H of O and LSE -- every step
-    e2e_steps = max(3, min(args.steps, 30))
+    # pinned memory, the kernel, D2H of O and LSE -- every step (the
+    # host-buffer entry point covers equal query and K/V head counts)
+    e2e_steps = max(3, min(args.steps, 30)) if not gqa else 0
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty_like(q).pin_memory()
     lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     wsp = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8,
                       device=dev)
-    for _ in range(2):
+    for _ in range(2 if e2e_steps else 0):
         fa.fa_fwd_host(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
     barrier(ws)
@@ -327,7 +331,7 @@ def run_ours(args, w, causal):
     if fa.fa_device_error() != 0:
         raise RuntimeError("device status set during the end-to-end leg")
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), ws)
-    e2e_value = aggregate_tflops(flops, e2e_steps, e2e_ms, ws)
+    e2e_value = aggregate_tflops(flops, e2e_steps, e2e_ms, ws) if e2e_steps else None
     tbytes = q.numel() * 2
     h2d = 3 * tbytes
     d2h = tbytes + B * H * N * 4
@@ -345,13 +349,13 @@ def run_ours(args, w, causal):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"bf16_tflops (burst) of {peak_kind}",
-                     "traffic": recorded_traffic(),
+                     "traffic": recorded_traffic() if w.name == "llama" else None,
                      "kernel": f"fa_fwd_kernel<{d},{str(causal).lower()}>",
                      "kernel_ms": kern_ms},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "ms_per_step": e2e_ms / e2e_steps,
-                "api": "fa_fwd_host (C ABI, pinned host buffers)"},
+        "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                 "ms_per_step": e2e_ms / e2e_steps,
+                 "api": "fa_fwd_host (C ABI, pinned host buffers)"} if e2e_steps else None),
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

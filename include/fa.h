@@ -74,6 +74,23 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
            fa_stream_t stream);
 
 /*
+ * fa_fwd_gqa -- grouped-query (and multi-query) attention: H query heads
+ * share H_kv key/value heads, query head h of batch b using K/V head
+ * h / (H / H_kv) ("Understanding FlashAttention Pt 1", section 4.1: the
+ * number of query heads is a multiple of the number of K/V heads).
+ *
+ *   Q, O     bf16 [B, H, N, d];  LSE fp32 [B, H, N]
+ *   K, V     bf16 [B, H_kv, N, d]
+ *   H_kv     >= 1 and divides H (H_kv = 1: multi-query; H_kv = H: fa_fwd)
+ * Everything else, including errors (FA_ERR_SHAPE when H_kv does not divide
+ * H), as fa_fwd.  Consecutive query heads of a group run next to each other
+ * so they share the group's K/V through L2.
+ */
+int fa_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
+               int B, int H, int H_kv, int N, int d, int causal, float scale,
+               fa_stream_t stream);
+
+/*
  * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs for this
  * shape: room for Q, K, V, O (bf16) and LSE (fp32), each 256-byte aligned.
  * Returns 0 for an invalid shape.

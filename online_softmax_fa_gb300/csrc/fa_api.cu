@@ -108,28 +108,30 @@ int record_message(int status, const char *what) {
 
 extern "C" {
 
-int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-           int N, int d, int causal, float scale, fa_stream_t stream) {
+int fa_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+               int H, int H_kv, int N, int d, int causal, float scale, fa_stream_t stream) {
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
     int rc = check_shape(B, H, N, d, scale);
     if (rc != FA_OK) return rc;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
     const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
     if (mis16(Q) || mis16(K) || mis16(V) || mis16(O) ||
         (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
         return FA_ERR_ALIGN;
-    const size_t n_elem = static_cast<size_t>(B) * H * N * d;
-    const size_t t_bytes = n_elem * 2, l_bytes = static_cast<size_t>(B) * H * N * 4;
-    for (const void *in : {Q, K, V})
-        if (overlaps(O, t_bytes, in, t_bytes) || overlaps(LSE, l_bytes, in, t_bytes))
+    const size_t q_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
+    const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
+    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(LSE, l_bytes, Q, q_bytes)) return FA_ERR_ALIAS;
+    for (const void *in : {K, V})
+        if (overlaps(O, q_bytes, in, kv_bytes) || overlaps(LSE, l_bytes, in, kv_bytes))
             return FA_ERR_ALIAS;
-    if (overlaps(O, t_bytes, LSE, l_bytes)) return FA_ERR_ALIAS;
+    if (overlaps(O, q_bytes, LSE, l_bytes)) return FA_ERR_ALIAS;
 
     rc = check_arch();
     if (rc != FA_OK) return rc;
     CUtensorMap tmQ, tmK, tmV;
-    const int BH = B * H;
-    if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, BH, N, d) ||
-        !encode_qkv_map(&tmV, V, BH, N, d))
+    if (!encode_qkv_map(&tmQ, Q, B * H, N, d) || !encode_qkv_map(&tmK, K, B * H_kv, N, d) ||
+        !encode_qkv_map(&tmV, V, B * H_kv, N, d))
         return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     fa::LaunchArgs a;
     a.tmQ = &tmQ;
@@ -137,14 +139,21 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int
     a.tmV = &tmV;
     a.O = O;
     a.LSE = LSE;
-    a.BH = BH;
+    a.BH = B * H;
     a.N = N;
     a.d = d;
+    a.H = H;
+    a.Hkv = H_kv;
     a.causal = causal != 0;
     a.scale = scale;
     a.limit_ns = kWaitLimitNs;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     return fa::launch_fwd(a);
+}
+
+int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+           int N, int d, int causal, float scale, fa_stream_t stream) {
+    return fa_fwd_gqa(Q, K, V, O, LSE, B, H, H, N, d, causal, scale, stream);
 }
 
 size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {

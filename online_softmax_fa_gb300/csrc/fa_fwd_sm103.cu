@@ -130,7 +130,9 @@ struct Params {
     __nv_bfloat16 *O;
     float *LSE;
     int N;
-    int BH;         // batch x heads
+    int BH;         // batch x query heads
+    int H;          // query heads per batch
+    int group;      // query heads per K/V head (grouped-query attention; 1 = MHA)
     int n_qblocks;  // ceil(N / 256)
     int n_ktiles;   // ceil(N / 128)
     int n_items;    // BH x n_qblocks
@@ -182,7 +184,7 @@ __device__ __forceinline__ SmemView<D> smem_view() {
 // needs 2*qb + 2 key tiles), heads interleaved; otherwise head-major (equal
 // cost, and consecutive items share K/V in L2).
 struct Work {
-    int bh, qb, n_sub0, n_sub1;  // n_sub1 >= n_sub0
+    int bh, kvh, qb, n_sub0, n_sub1;  // kvh: K/V head row; n_sub1 >= n_sub0
 };
 
 template <bool CAUSAL>
@@ -195,6 +197,11 @@ __device__ __forceinline__ Work work_of(const Params &p, int x) {
         w.bh = x / p.n_qblocks;
         w.qb = x % p.n_qblocks;
     }
+    // grouped-query attention: query head h of batch b reads K/V head
+    // h / group of that batch (consecutive query heads share one K/V head,
+    // and the schedule keeps them adjacent, so they share it in L2)
+    const int b = w.bh / p.H, h = w.bh - b * p.H;
+    w.kvh = b * (p.H / p.group) + h / p.group;
     const int T = p.n_ktiles, N = p.N;
     // key tiles each 128-row sub-tile needs (causal: up to its last row)
     w.n_sub0 = CAUSAL ? min(T, min(w.qb * kBlockM + kSubM - 1, N - 1) / kBlockN + 1) : T;
@@ -251,7 +258,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
             mbar_arrive_expect_tx(&v.k_full[s], C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(v.k + s * C::kTileBytes + c * kBoxBytes, tmK, &v.k_full[s], 64 * c,
-                            j * kBlockN, w.bh, pol_kv);
+                            j * kBlockN, w.kvh, pol_kv);
             if (t >= C::kStages) ok = mbar_wait(&v.v_empty[s], ph ^ 1, ctl, kSiteVEmpty);
             if (!ok) {  // K of tile t is in flight: count it for the drain
                 g = t + 1;
@@ -260,7 +267,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
             mbar_arrive_expect_tx(&v.v_full[s], C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(v.v + s * C::kTileBytes + c * kBoxBytes, tmV, &v.v_full[s], 64 * c,
-                            j * kBlockN, w.bh, pol_kv);
+                            j * kBlockN, w.kvh, pol_kv);
         }
         if (ok) g += w.n_sub1;
     }
@@ -648,6 +655,8 @@ static int launch_t(const LaunchArgs &a) {
     p.LSE = a.LSE;
     p.N = a.N;
     p.BH = a.BH;
+    p.H = a.H;
+    p.group = a.H / a.Hkv;
     p.n_qblocks = (a.N + kBlockM - 1) / kBlockM;
     p.n_ktiles = (a.N + kBlockN - 1) / kBlockN;
     const long long items = static_cast<long long>(p.n_qblocks) * a.BH;

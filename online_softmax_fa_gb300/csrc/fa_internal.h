@@ -16,6 +16,7 @@ struct LaunchArgs {
     void *O;
     float *LSE;
     int BH, N, d;
+    int H, Hkv;  // query heads and K/V heads per batch (H % Hkv == 0)
     bool causal;
     float scale;
     uint64_t limit_ns;  // bound on every in-kernel wait

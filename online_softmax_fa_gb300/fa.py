@@ -42,6 +42,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
     lib.fa_fwd.restype = I
+    lib.fa_fwd_gqa.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+    lib.fa_fwd_gqa.restype = I
     lib.fa_fwd_host_workspace_bytes.argtypes = [I, I, I, I]
     lib.fa_fwd_host_workspace_bytes.restype = S
     lib.fa_fwd_host.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
@@ -104,6 +106,33 @@ def fa_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None 
                                float(scale), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_gqa(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+               stream=None):
+    """Grouped-query attention: q [B, H, N, d]; k, v [B, H_kv, N, d] with
+    H_kv dividing H.  Returns (o [B, H, N, d] bf16, lse [B, H, N] fp32)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda \
+                or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 [B, H, N, d] tensor")
+    B, H, N, d = (int(x) for x in q.shape)
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    H_kv = int(k.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, H_kv, N, d, 1 if causal else 0,
+                                   float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_gqa")
     return o, lse
 
 

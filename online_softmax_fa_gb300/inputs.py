@@ -16,13 +16,16 @@ llama  1, 32, 8192, 128            yes     i.i.d. N(0,1) (Llama-3-8B layer shape
 batch  16, 16, 2048, 128           no      i.i.d. N(0,1)
 long   1, 8, 32771, 128            yes     i.i.d. N(0,1); N = 256*128 + 3 leaves a
                                            ragged tail; checked on sampled rows
+llama_ 1, 32 (8 K/V), 8192, 128    yes     i.i.d. N(0,1); grouped-query heads
+gqa
 =====  ==========================  ======  ======================================
 
 Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draw Q, then K, then V
-with ``torch.randn(B, H, N, d, dtype=float32)``; apply the K row scaling (the
+with ``torch.randn(B, H, N, d, dtype=float32)`` (K and V with H_kv heads for
+grouped-query workloads); apply the K row scaling (the
 ``late`` workload only, j the 0-based key position inside each head) in
 fp32; round to bf16 (round-to-nearest-even).  Default seeds: tiny 1, late 2,
-llama 3, batch 4, long 5.  No public dataset is involved: the workloads are
+llama 3, batch 4, long 5, llama_gqa 6.  No public dataset is involved: the workloads are
 shapes, and random N(0,1) values stand in for activations.
 """
 from __future__ import annotations
@@ -44,11 +47,16 @@ class Workload:
     seed: int
     k_row_ramp: bool = False  # K row j scaled by (1 + 4j/N)
     sampled_rows: int = 0  # >0: parity on this many seeded rows per head
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
 
     @property
     def scale(self) -> float:
         # 1/sqrt(d) rounded to fp32: the value both sides receive.
         return float(np.float32(1.0 / np.sqrt(self.d)))
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     def flops(self, causal: bool) -> float:
         """Nominal forward FLOPs 4*B*H*N^2*d, halved when causal."""
@@ -62,18 +70,22 @@ WORKLOADS = {
     "llama": Workload("llama", 1, 32, 8192, 128, (True,), 3),
     "batch": Workload("batch", 16, 16, 2048, 128, (False,), 4),
     "long": Workload("long", 1, 8, 32771, 128, (True,), 5, sampled_rows=512),
+    # Llama-3-8B's own head layout: 32 query heads share 8 K/V heads
+    "llama_gqa": Workload("llama_gqa", 1, 32, 8192, 128, (True,), 6, H_kv=8),
 }
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int,
-             k_row_ramp: bool = False):
-    """Q, K, V as contiguous CPU bf16 tensors [B, H, N, d] (see the recipe)."""
+             k_row_ramp: bool = False, H_kv: int = 0):
+    """Q [B, H, N, d] and K, V [B, H_kv or H, N, d] as contiguous CPU bf16
+    tensors (see the recipe)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     shape = (B, H, N, d)
+    kv_shape = (B, H_kv or H, N, d)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
     if k_row_ramp:
         j = torch.arange(N, dtype=torch.float32)
         k = k * (1.0 + 4.0 * j / N).view(1, 1, N, 1)
@@ -82,7 +94,7 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int,
 
 
 def make_workload(w: Workload):
-    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.k_row_ramp)
+    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.k_row_ramp, w.H_kv)
 
 
 def fixed_edge_rows(N: int, tile: int = 128) -> list:

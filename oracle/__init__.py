@@ -142,6 +142,26 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None,
     return O.reshape(*lead, R, dv), LSE.reshape(*lead, R)
 
 
+def attention_fwd_gqa(q, k, v, causal: bool = False, scale: float | None = None,
+                      rows=None, nthreads: int | None = None):
+    """Grouped-query attention by its definition ("Understanding
+    FlashAttention Pt 1", section 4.1): q [B, H, N, d], k/v [B, H_kv, N, d]
+    with H_kv dividing H; query head h uses K/V head h // (H / H_kv).  Each
+    K/V head is repeated for its group and the dense oracle runs on the
+    result.  Returns (O [B, H, R, dv], LSE [B, H, R])."""
+    q, k, v = _as_f64(q, "q"), _as_f64(k, "k"), _as_f64(v, "v")
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape[:3] + (k.shape[3],):
+        raise ValueError("expected q [B,H,N,d] and k, v [B,H_kv,N,*]")
+    H, H_kv = q.shape[1], k.shape[1]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError(f"H_kv={H_kv} does not divide H={H}")
+    group = H // H_kv
+    k_full = np.repeat(k, group, axis=1)  # head h -> K/V head h // group
+    v_full = np.repeat(v, group, axis=1)
+    return attention_fwd(q, k_full, v_full, causal=causal, scale=scale, rows=rows,
+                         nthreads=nthreads)
+
+
 def attention_fwd_blockwise(q, k, v, bounds, causal: bool = False,
                             scale: float | None = None, reverse: bool = False,
                             rows=None, nthreads: int | None = None,

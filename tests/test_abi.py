@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("fa_fwd", "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_device_error",
+    for must in ("fa_fwd", "fa_fwd_gqa", "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_device_error",
                  "fa_status_string", "fa_selftest_bounded_wait", "fa_version"):
         assert must in names
 
@@ -117,3 +117,12 @@ def test_binding_fails_loudly_without_library(tmp_path):
             fa.load_library(str(tmp_path / "missing.so"))
     finally:
         fa._lib = saved
+
+
+def test_gqa_argument_checks(lib):
+    base = (16, 32, 48, 4096, 8192)
+    # H_kv must divide H and be >= 1
+    assert lib.fa_fwd_gqa(*base, 1, 8, 3, 8, 64, 0, 0.125, None) == -2
+    assert lib.fa_fwd_gqa(*base, 1, 8, 0, 8, 64, 0, 0.125, None) == -2
+    assert lib.fa_fwd_gqa(None, 32, 48, 4096, 8192, 1, 8, 2, 8, 64, 0, 0.125, None) == -1
+    assert lib.fa_fwd_gqa(*base, 1, 8, 2, 8, 96, 0, 0.125, None) == -3

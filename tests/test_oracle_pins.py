@@ -304,3 +304,37 @@ def test_bad_arguments_rejected():
         oracle.attention_fwd_blockwise(q, q, q, [0, 2, 2, 4])
     with pytest.raises(ValueError):
         oracle.attention_fwd_blockwise(q, q, q, [0, 3])
+
+
+# ------------------------------------------------- grouped-query attention
+def test_gqa_head_mapping_closed_form():
+    """Query head h reads K/V head h // (H / H_kv): with identical keys per
+    K/V head, O of query head h is the mean of that K/V head's values."""
+    rng = np.random.default_rng(30)
+    B, H, H_kv, N, d = 2, 6, 3, 17, 4
+    q = rng.standard_normal((B, H, N, d))
+    k = np.broadcast_to(rng.standard_normal((B, H_kv, 1, d)), (B, H_kv, N, d)).copy()
+    v = rng.standard_normal((B, H_kv, N, d)) + np.arange(H_kv).reshape(1, H_kv, 1, 1) * 10
+    O, _ = oracle.attention_fwd_gqa(q, k, v, scale=0.3)
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(O[b, h], np.broadcast_to(v[b, h // 2].mean(0), (N, d)),
+                                       atol=1e-12)
+
+
+def test_gqa_reduces_to_mha_and_mqa():
+    rng = np.random.default_rng(31)
+    q, k, v = (rng.standard_normal((1, 4, 23, 8)) for _ in range(3))
+    O1, L1 = oracle.attention_fwd_gqa(q, k, v, causal=True)
+    O2, L2 = oracle.attention_fwd(q, k, v, causal=True)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+    # one K/V head (multi-query): every query head attends to the same K/V
+    k1, v1 = k[:, :1], v[:, :1]
+    Om, Lm = oracle.attention_fwd_gqa(q, k1, v1)
+    for h in range(4):
+        Oh, Lh = oracle.attention_fwd(q[:, h:h + 1], k1, v1)
+        np.testing.assert_array_equal(Om[:, h:h + 1], Oh)
+        np.testing.assert_array_equal(Lm[:, h:h + 1], Lh)
+    with pytest.raises(ValueError):
+        oracle.attention_fwd_gqa(q, k[:, :3], v[:, :3])

@@ -202,3 +202,45 @@ def test_bounded_wait_expires_with_status(fa):
     o, lse = run(fa, q, k, v, False, 0.125)
     O_ref, L_ref = oracle.attention_fwd(q, k, v, scale=0.125)
     check(o, lse, O_ref, L_ref, "after selftest")
+
+
+# ------------------------------------------------- grouped-query attention
+@pytest.mark.parametrize("H,H_kv,N,d,causal", [
+    (8, 2, 1000, 128, True), (8, 2, 1000, 128, False), (6, 1, 300, 64, True),
+    (4, 4, 257, 64, False), (32, 8, 520, 128, True)])
+def test_gqa_parity(fa, H, H_kv, N, d, causal):
+    q, k, v = make_qkv(2, H, N, d, seed=40 + H + H_kv + N, H_kv=H_kv)
+    dev = torch.device("cuda")
+    o, lse = fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale_of(d))
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    O_ref, L_ref = oracle.attention_fwd_gqa(q, k, v, causal=causal, scale=scale_of(d))
+    check(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref,
+          f"gqa H={H} H_kv={H_kv} N={N} d={d} causal={causal}")
+
+
+def test_gqa_with_equal_heads_is_fa_fwd(fa):
+    q, k, v = make_qkv(1, 4, 700, 128, seed=50)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o1, l1 = fa.fa_fwd_gqa(q, k, v, causal=True)
+    o2, l2 = fa.fa_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_llama_gqa_workload_sampled(fa):
+    w = WORKLOADS["llama_gqa"]
+    q, k, v = make_workload(w)
+    dev = torch.device("cuda")
+    o_d, lse_d = fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    assert torch.isfinite(lse_d).all() and torch.isfinite(o_d.float()).all()
+    rows = sample_rows(w.N, w.H, 32, seed=w.seed)
+    O_ref, L_ref = oracle.attention_fwd_gqa(q, k, v, causal=True, scale=w.scale,
+                                            rows=rows)
+    idx = np.arange(w.H)[:, None]
+    o = o_d.float()[0].cpu().numpy()
+    lse = lse_d[0].cpu().numpy()
+    check(o[idx, rows][None], lse[idx, rows][None], O_ref, L_ref, "llama_gqa")
