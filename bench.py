@@ -38,7 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from online_softmax_fa_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
+from online_softmax_fa_gb300.inputs import (DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
+                                            make_decode, make_workload)
 
 METRIC = ("attn fwd TFLOP/s (4·B·H·N²·d, causal halved) "
           "and % of GB300 BF16 tensor peak")
@@ -364,13 +365,84 @@ def run_ours(args, w, causal):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------ decode leg
+def decode_bytes(w, n_states: int) -> int:
+    """Algorithmic HBM bytes of one decoding step: K and V read once per K/V
+    head, q read and O written, LSE written, and each split's softmax state
+    (d + 2 floats) written by the split kernel and read by the merge."""
+    kv = 2 * w.B * w.kv_heads * w.N * w.d * 2
+    qo = 2 * w.B * w.H * w.d * 2
+    return kv + qo + w.B * w.H * 4 + 2 * n_states * (w.d + 2) * 4
+
+
+def run_decode(args, w):
+    import torch
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from online_softmax_fa_gb300 import fa
+    from online_softmax_fa_gb300.build import build_library
+    build_library()
+    fa.load_library()
+    q, k, v = make_decode(w.B, w.H, w.kv_heads, w.N, w.d, w.seed)
+    need = fa.fa_decode_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d)
+    sets = [(q.to(dev), k.to(dev), v.to(dev),
+             torch.empty(need, dtype=torch.uint8, device=dev),
+             torch.empty_like(q, device=dev),
+             torch.empty((w.B, w.H), dtype=torch.float32, device=dev)) for _ in range(3)]
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        qd, kd, vd, wk, od, ld = sets[i % 3]
+        fa.fa_decode(qd, kd, vd, wk, od, ld, scale=w.scale)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws_)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        qd, kd, vd, wk, od, ld = sets[i % 3]
+        fa.fa_decode(qd, kd, vd, wk, od, ld, scale=w.scale)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_)
+    if fa.fa_device_error() != 0:
+        raise RuntimeError("device status set during the decode leg")
+    ms = max_over_ranks(e0.elapsed_time(e1), ws_) / args.steps
+    if rank != 0:
+        return
+    # states: B*H_kv*n_splits*G = workspace floats / (d + 2), from the layout
+    n_states = need // 4 // (w.d + 2)
+    nbytes = decode_bytes(w, n_states)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    flops = 4.0 * w.B * w.H * w.N * w.d
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            hbm, kind = float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        hbm, kind = 6800.0, "fallback"
+    out = {"metric": "attn decode TFLOP/s (4·B·H·N·d) at one query row per head",
+           "value": ws_ * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": ws_,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"decode B{w.B} H{w.H} (K/V heads {w.kv_heads}) "
+                                  f"N{w.N} d{w.d}, one query row per head",
+                      "l2": "inputs > L2: 3 resident K/V caches of 537 MB in rotation"},
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                        "frac": gbs / hbm, "peak_source": f"hbm_gbs of {kind}",
+                        "traffic": None, "algorithmic_bytes": nbytes},
+           "gpu_launches": 2 * args.steps}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS),
+                    default="llama")
     ap.add_argument("--causal", choices=["auto", "0", "1"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -378,6 +450,9 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.steps < 1:
         ap.error("--steps must be >= 1")
+    if args.workload in DECODE_WORKLOADS:
+        run_decode(args, DECODE_WORKLOADS[args.workload])
+        return
     w = WORKLOADS[args.workload]
     causal = w.causal[-1] if args.causal == "auto" else args.causal == "1"
     ws, rank, local = dist_env()

@@ -119,6 +119,39 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host,
                 int causal, float scale, fa_stream_t stream);
 
 /*
+ * fa_decode_workspace_bytes -- device workspace fa_decode needs: the
+ * per-split softmax states (m, l and the d-wide accumulator for every
+ * query head and key split).  Returns 0 for an invalid or unsupported shape.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int N, int d);
+
+/*
+ * fa_decode -- one new query row per (batch, query head) against a
+ * key/value cache: O = softmax(scale * q K^T) V and LSE, every cached key
+ * visible.  Decoding has no query-block parallelism ("FlashAttention-2 --
+ * Deeper Math", "What FA-2 does not fix"), so the keys are split across
+ * warps, each keeps the online-softmax state of "Understanding
+ * FlashAttention Pt 1", section 2.4, for its split, and a second kernel
+ * merges the splits with the same rule.
+ *
+ *   Q, O     bf16 [B, H, d] (the newest token of each sequence and head)
+ *   K, V     bf16 [B, H_kv, N, d], N cached positions
+ *   LSE      fp32 [B, H]
+ *   H_kv     divides H; H / H_kv in {1, 2, 4, 8} (FA_ERR_UNSUPPORTED else);
+ *            each K/V row is read once for all query heads of its group
+ *   d        64 or 128; B * H_kv <= 65535
+ *   workspace  caller-owned device memory of at least
+ *            fa_decode_workspace_bytes(B, H, H_kv, N, d) bytes, 256-byte
+ *            aligned; its contents are scratch and it must not overlap the
+ *            other buffers
+ * Checks, errors and asynchrony as fa_fwd (FA_ERR_WORKSPACE for a missing,
+ * small or misaligned workspace).  Two kernels run on `stream`.
+ */
+int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
+              void *workspace, size_t workspace_bytes, int B, int H, int H_kv,
+              int N, int d, float scale, fa_stream_t stream);
+
+/*
  * fa_device_error -- synchronises `stream`, then reads and clears the
  * library's device status word on the current device.  Returns FA_OK, or
  * FA_ERR_TIMEOUT if a kernel since the last call gave up on a bounded wait

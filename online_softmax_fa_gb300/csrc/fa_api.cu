@@ -192,6 +192,83 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
     return FA_OK;
 }
 
+// ----------------------------------------------------------- decoding
+namespace {
+int check_decode_shape(int B, int H, int H_kv, int N, int d, float scale) {
+    if (B < 1 || H < 1 || H_kv < 1 || N < 1) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+    if (H % H_kv != 0) return FA_ERR_SHAPE;
+    const int G = H / H_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H_kv > 65535) return FA_ERR_SHAPE;  // grid.y
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_SCALE;
+    return FA_OK;
+}
+
+// workspace layout: partial accumulators, then partial (m, l) pairs
+void decode_layout(int B, int H, int H_kv, int N, int d, size_t *acc_bytes, size_t *ml_bytes) {
+    const size_t states = static_cast<size_t>(B) * H_kv * fa::decode_n_splits(B, H_kv, N) *
+                          (H / H_kv);
+    *acc_bytes = align256(states * d * sizeof(float));
+    *ml_bytes = align256(states * 2 * sizeof(float));
+}
+}  // namespace
+
+size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int N, int d) {
+    if (check_decode_shape(B, H, H_kv, N, d, 1.f) != FA_OK) return 0;
+    size_t a = 0, m = 0;
+    decode_layout(B, H, H_kv, N, d, &a, &m);
+    return a + m;
+}
+
+int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
+              void *workspace, size_t workspace_bytes, int B, int H, int H_kv, int N, int d,
+              float scale, fa_stream_t stream) {
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
+    int rc = check_decode_shape(B, H, H_kv, N, d, scale);
+    if (rc != FA_OK) return rc;
+    const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (mis16(Q) || mis16(K) || mis16(V) || mis16(O) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+        return FA_ERR_ALIGN;
+    size_t acc_bytes = 0, ml_bytes = 0;
+    decode_layout(B, H, H_kv, N, d, &acc_bytes, &ml_bytes);
+    if (!workspace || workspace_bytes < acc_bytes + ml_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_WORKSPACE;
+    const size_t q_bytes = static_cast<size_t>(B) * H * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
+    const size_t l_bytes = static_cast<size_t>(B) * H * 4;
+    const size_t w_bytes = acc_bytes + ml_bytes;
+    const struct { const void *p; size_t n; } ins[] = {{Q, q_bytes}, {K, kv_bytes},
+                                                       {V, kv_bytes}};
+    for (const auto &in : ins)
+        if (overlaps(O, q_bytes, in.p, in.n) || overlaps(LSE, l_bytes, in.p, in.n) ||
+            overlaps(workspace, w_bytes, in.p, in.n))
+            return FA_ERR_ALIAS;
+    if (overlaps(O, q_bytes, LSE, l_bytes) || overlaps(O, q_bytes, workspace, w_bytes) ||
+        overlaps(LSE, l_bytes, workspace, w_bytes))
+        return FA_ERR_ALIAS;
+    rc = check_arch();
+    if (rc != FA_OK) return rc;
+    fa::DecodeArgs a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.LSE = LSE;
+    a.part_acc = static_cast<float *>(workspace);
+    a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + acc_bytes);
+    a.B = B;
+    a.H = H;
+    a.H_kv = H_kv;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return fa::launch_decode(a);
+}
+
 int fa_device_error(fa_stream_t stream) {
     int v = 0;
     const int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);

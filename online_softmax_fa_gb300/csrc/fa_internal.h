@@ -25,6 +25,20 @@ struct LaunchArgs {
 
 int launch_fwd(const LaunchArgs &a);
 
+// Split-KV decoding (fa_decode_sm103.cu).
+struct DecodeArgs {
+    const void *Q, *K, *V;  // bf16 [B,H,d], [B,H_kv,N,d], [B,H_kv,N,d]
+    void *O;                // bf16 [B,H,d]
+    float *LSE;             // fp32 [B,H]
+    float *part_acc;        // fp32 [B*H_kv, n_splits, G, d]
+    float *part_ml;         // fp32 [B*H_kv, n_splits, G, 2]
+    int B, H, H_kv, N, d;
+    float scale;
+    cudaStream_t stream;
+};
+int launch_decode(const DecodeArgs &a);
+int decode_n_splits(int B, int H_kv, int N);
+
 // Records the CUDA error of a failed call (thread-local) for
 // fa_last_error_detail(); returns FA_ERR_LAUNCH.
 int record_cuda_error(cudaError_t e, const char *what);

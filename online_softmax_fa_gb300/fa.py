@@ -48,6 +48,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_host_workspace_bytes.restype = S
     lib.fa_fwd_host.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
     lib.fa_fwd_host.restype = I
+    lib.fa_decode_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.fa_decode_workspace_bytes.restype = S
+    lib.fa_decode.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
+    lib.fa_decode.restype = I
     lib.fa_device_error.argtypes = [P]
     lib.fa_device_error.restype = I
     lib.fa_selftest_bounded_wait.argtypes = [I, P]
@@ -155,6 +159,42 @@ def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, workspace,
         B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_host")
+
+
+def fa_decode_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(load_library().fa_decode_workspace_bytes(B, H, H_kv, N, d))
+
+
+def fa_decode(q, k, v, workspace=None, o=None, lse=None, scale: float | None = None,
+              stream=None):
+    """Decoding step: q [B, H, d] (newest token), k/v cache [B, H_kv, N, d].
+    Returns (o [B, H, d] bf16, lse [B, H] fp32).  ``workspace``: CUDA uint8
+    tensor of at least fa_decode_workspace_bytes(...) bytes (allocated when
+    not given)."""
+    import torch
+    if q.dim() != 3 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B, H, d] and k, v [B, H_kv, N, d]")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    B, H, d = (int(x) for x in q.shape)
+    H_kv, N = int(k.shape[1]), int(k.shape[2])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = fa_decode_workspace_bytes(B, H, H_kv, N, d)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), B, H, H_kv,
+                                  N, d, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_decode")
+    return o, lse
 
 
 def fa_device_error(stream=None) -> int:

@@ -18,6 +18,8 @@ long   1, 8, 32771, 128            yes     i.i.d. N(0,1); N = 256*128 + 3 leaves
                                            ragged tail; checked on sampled rows
 llama_ 1, 32 (8 K/V), 8192, 128    yes     i.i.d. N(0,1); grouped-query heads
 gqa
+decode 16, 32 (8 K/V), 8192, 128   n/a     one query row per head against an
+                                           8192-position K/V cache (seed 7)
 =====  ==========================  ======  ======================================
 
 Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draw Q, then K, then V
@@ -73,6 +75,24 @@ WORKLOADS = {
     # Llama-3-8B's own head layout: 32 query heads share 8 K/V heads
     "llama_gqa": Workload("llama_gqa", 1, 32, 8192, 128, (True,), 6, H_kv=8),
 }
+
+# Decoding: one new query row per (sequence, head) against a K/V cache of N
+# positions; a batch of 16 Llama-3-8B sequences (32 query / 8 K/V heads).
+DECODE_WORKLOADS = {
+    "decode": Workload("decode", 16, 32, 8192, 128, (False,), 7, H_kv=8),
+}
+
+
+def make_decode(B: int, H: int, H_kv: int, N: int, d: int, seed: int):
+    """q [B, H, d] (the newest token), then K, V [B, H_kv, N, d], drawn in
+    that order as fp32 N(0,1) and rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H_kv, N, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H_kv, N, d), generator=g, dtype=torch.float32)
+    return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
+            v.to(torch.bfloat16).contiguous())
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int,

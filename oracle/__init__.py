@@ -57,6 +57,10 @@ def _load():
                                       ctypes.c_int, ctypes.c_double, p, i64,
                                       ctypes.c_int]
         lib.fa_oracle_fwd.restype = ctypes.c_int
+        lib.fa_oracle_fwd_q.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64,
+                                        ctypes.c_int, ctypes.c_double, p, i64,
+                                        ctypes.c_int]
+        lib.fa_oracle_fwd_q.restype = ctypes.c_int
         lib.fa_oracle_fwd_blockwise.argtypes = [
             p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
             p, i64, p, i64, ctypes.c_int, p, p, p, ctypes.c_int]
@@ -160,6 +164,38 @@ def attention_fwd_gqa(q, k, v, causal: bool = False, scale: float | None = None,
     v_full = np.repeat(v, group, axis=1)
     return attention_fwd(q, k_full, v_full, causal=causal, scale=scale, rows=rows,
                          nthreads=nthreads)
+
+
+def attention_decode(q, k, v, causal: bool = True, scale: float | None = None,
+                     nthreads: int | None = None):
+    """Attention of the newest query rows against a key/value cache, by the
+    definition: q [B, H, Nq, d] are the last Nq positions of a sequence whose
+    keys and values are k, v [B, H_kv, N, d] (H_kv divides H; query head h
+    uses K/V head h // (H / H_kv)).  Causal keeps key j for query row i iff
+    j <= i + (N - Nq); with Nq = 1 every key is kept.
+    Returns (O [B, H, Nq, dv], LSE [B, H, Nq])."""
+    q, k, v = _as_f64(q, "q"), _as_f64(k, "k"), _as_f64(v, "v")
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4 or k.shape[:3] != v.shape[:3]:
+        raise ValueError("expected q [B,H,Nq,d] and k, v [B,H_kv,N,*]")
+    B, H, Nq, d = q.shape
+    H_kv, N = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or H_kv < 1 or H % H_kv:
+        raise ValueError("shape mismatch")
+    group = H // H_kv
+    k_full = np.ascontiguousarray(np.repeat(k, group, axis=1))
+    v_full = np.ascontiguousarray(np.repeat(v, group, axis=1))
+    dv = v.shape[3]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q = np.ascontiguousarray(q)
+    O = np.empty((B * H, Nq, dv), dtype=np.float64)
+    LSE = np.empty((B * H, Nq), dtype=np.float64)
+    rc = _load().fa_oracle_fwd_q(_ptr(q), _ptr(k_full), _ptr(v_full), _ptr(O), _ptr(LSE),
+                                 B * H, Nq, N, d, dv, 1 if causal else 0, float(scale),
+                                 None, Nq, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"fa_oracle_fwd_q failed ({rc})")
+    return O.reshape(B, H, Nq, dv), LSE.reshape(B, H, Nq)
 
 
 def attention_fwd_blockwise(q, k, v, bounds, causal: bool = False,

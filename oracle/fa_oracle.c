@@ -38,6 +38,8 @@
  * at the end; plus the fully-masked-block guard of gowda.ai Listing 26.3.
  *
  * Layouts: Q, K are [BH, N, d]; V is [BH, N, dv]; all row-major fp64.
+ * fa_oracle_fwd_q() takes Q as [BH, Nq, d] with Nq <= N query rows that
+ * sit at the last Nq positions (decoding: Nq = 1 is the newest token).
  * rows == NULL computes every query row: O is [BH, N, dv], LSE is [BH, N].
  * rows != NULL is a [BH, R] table of query indices: O is [BH, R, dv],
  * LSE is [BH, R].  Work is spread over nthreads POSIX threads; each output
@@ -71,6 +73,7 @@ typedef struct {
     const double *Q, *K, *V;
     double *O, *LSE;
     int64_t BH, N, d, dv, R;
+    int64_t Nq;   /* query rows per head (== N for self-attention) */
     const int64_t *rows; /* NULL -> all rows */
     int causal;
     double scale;
@@ -93,7 +96,7 @@ static int64_t query_index(const oracle_job *jb, int64_t bh, int64_t r) {
 static int dense_chunk(oracle_job *jb, int64_t bh, int64_t r0, int64_t r1,
                        double *S, double *P) {
     const int64_t N = jb->N, d = jb->d, dv = jb->dv;
-    const double *Qh = jb->Q + bh * N * d;
+    const double *Qh = jb->Q + bh * jb->Nq * d;
     const double *Kh = jb->K + bh * N * d;
     const double *Vh = jb->V + bh * N * dv;
     const int64_t nr = r1 - r0;
@@ -107,7 +110,8 @@ static int dense_chunk(oracle_job *jb, int64_t bh, int64_t r0, int64_t r1,
             const double *k = Kh + j * d;
             for (int64_t c = 0; c < d; ++c) dot += q[c] * k[c];
             S[r * N + j] = jb->scale * dot;
-            if (jb->causal && j > i) S[r * N + j] = -INFINITY;
+            /* query row i sits at key position i + (N - Nq) */
+            if (jb->causal && j > i + (N - jb->Nq)) S[r * N + j] = -INFINITY;
         }
     }
     /* step 3: row max, probabilities, normaliser;  step 4: output, LSE */
@@ -144,7 +148,7 @@ static void blockwise_row(oracle_job *jb, int64_t bh, int64_t r, double *s,
                           double *a) {
     const int64_t N = jb->N, d = jb->d, dv = jb->dv;
     const int64_t i = query_index(jb, bh, r);
-    const double *q = jb->Q + (bh * N + i) * d;
+    const double *q = jb->Q + (bh * jb->Nq + i) * d;
     const double *Kh = jb->K + bh * N * d;
     const double *Vh = jb->V + bh * N * dv;
 
@@ -160,7 +164,7 @@ static void blockwise_row(oracle_job *jb, int64_t bh, int64_t r, double *s,
             double dot = 0.0;
             const double *k = Kh + j * d;
             for (int64_t c = 0; c < d; ++c) dot += q[c] * k[c];
-            s[j - j0] = (jb->causal && j > i) ? -INFINITY : jb->scale * dot;
+            s[j - j0] = (jb->causal && j > i + (N - jb->Nq)) ? -INFINITY : jb->scale * dot;
             if (s[j - j0] > m_b) m_b = s[j - j0];
         }
         if (m_b == -INFINITY) continue; /* block has no scores: no change */
@@ -266,30 +270,42 @@ static int run_threads(oracle_job *jb, void *(*fn)(void *), int nthreads) {
 
 static int check_common(const double *Q, const double *K, const double *V,
                         const double *O, const double *LSE, int64_t BH,
-                        int64_t N, int64_t d, int64_t dv, const int64_t *rows,
-                        int64_t R) {
+                        int64_t Nq, int64_t N, int64_t d, int64_t dv,
+                        const int64_t *rows, int64_t R) {
     if (!Q || !K || !V || !O || !LSE) return -1;
-    if (BH < 1 || N < 1 || d < 1 || dv < 1) return -1;
+    if (BH < 1 || N < 1 || Nq < 1 || Nq > N || d < 1 || dv < 1) return -1;
     if (rows) {
         if (R < 1) return -1;
         for (int64_t t = 0; t < BH * R; ++t)
-            if (rows[t] < 0 || rows[t] >= N) return -1;
+            if (rows[t] < 0 || rows[t] >= Nq) return -1;
     }
     return 0;
+}
+
+/* Nq query rows (Q is [BH, Nq, d]) against N keys (K, V are [BH, N, *]),
+ * Nq <= N.  Causal keeps key j for query row i iff j <= i + (N - Nq): the
+ * query rows are the last Nq positions of the sequence (with Nq == N this
+ * is j <= i).  rows index the Nq query rows. */
+int fa_oracle_fwd_q(const double *Q, const double *K, const double *V, double *O,
+                    double *LSE, int64_t BH, int64_t Nq, int64_t N, int64_t d, int64_t dv,
+                    int causal, double scale, const int64_t *rows, int64_t R,
+                    int nthreads) {
+    if (check_common(Q, K, V, O, LSE, BH, Nq, N, d, dv, rows, R)) return -1;
+    oracle_job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.Q = Q; jb.K = K; jb.V = V; jb.O = O; jb.LSE = LSE;
+    jb.BH = BH; jb.N = N; jb.Nq = Nq; jb.d = d; jb.dv = dv;
+    jb.rows = rows; jb.R = rows ? R : Nq;
+    jb.causal = causal ? 1 : 0; jb.scale = scale;
+    return run_threads(&jb, dense_worker, nthreads);
 }
 
 int fa_oracle_fwd(const double *Q, const double *K, const double *V, double *O,
                   double *LSE, int64_t BH, int64_t N, int64_t d, int64_t dv,
                   int causal, double scale, const int64_t *rows, int64_t R,
                   int nthreads) {
-    if (check_common(Q, K, V, O, LSE, BH, N, d, dv, rows, R)) return -1;
-    oracle_job jb;
-    memset(&jb, 0, sizeof jb);
-    jb.Q = Q; jb.K = K; jb.V = V; jb.O = O; jb.LSE = LSE;
-    jb.BH = BH; jb.N = N; jb.d = d; jb.dv = dv;
-    jb.rows = rows; jb.R = rows ? R : N;
-    jb.causal = causal ? 1 : 0; jb.scale = scale;
-    return run_threads(&jb, dense_worker, nthreads);
+    return fa_oracle_fwd_q(Q, K, V, O, LSE, BH, N, N, d, dv, causal, scale, rows, R,
+                           nthreads);
 }
 
 int fa_oracle_fwd_blockwise(const double *Q, const double *K, const double *V,
@@ -299,7 +315,7 @@ int fa_oracle_fwd_blockwise(const double *Q, const double *K, const double *V,
                             const int64_t *bounds, int64_t nblocks, int reverse,
                             double *M_out, double *L_out, double *A_out,
                             int nthreads) {
-    if (check_common(Q, K, V, O, LSE, BH, N, d, dv, rows, R)) return -1;
+    if (check_common(Q, K, V, O, LSE, BH, N, N, d, dv, rows, R)) return -1;
     if (!bounds || nblocks < 1 || bounds[0] != 0 || bounds[nblocks] != N) return -1;
     for (int64_t b = 0; b < nblocks; ++b)
         if (bounds[b + 1] <= bounds[b]) return -1;
@@ -307,7 +323,7 @@ int fa_oracle_fwd_blockwise(const double *Q, const double *K, const double *V,
     memset(&jb, 0, sizeof jb);
     jb.Q = Q; jb.K = K; jb.V = V; jb.O = O; jb.LSE = LSE;
     jb.BH = BH; jb.N = N; jb.d = d; jb.dv = dv;
-    jb.rows = rows; jb.R = rows ? R : N;
+    jb.rows = rows; jb.R = rows ? R : N; jb.Nq = N;
     jb.causal = causal ? 1 : 0; jb.scale = scale;
     jb.bounds = bounds; jb.nblocks = nblocks; jb.reverse = reverse ? 1 : 0;
     jb.M_out = M_out; jb.L_out = L_out; jb.A_out = A_out;

@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("fa_fwd", "fa_fwd_gqa", "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_device_error",
+    for must in ("fa_fwd", "fa_fwd_gqa", "fa_decode", "fa_decode_workspace_bytes", "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_device_error",
                  "fa_status_string", "fa_selftest_bounded_wait", "fa_version"):
         assert must in names
 
@@ -126,3 +126,20 @@ def test_gqa_argument_checks(lib):
     assert lib.fa_fwd_gqa(*base, 1, 8, 0, 8, 64, 0, 0.125, None) == -2
     assert lib.fa_fwd_gqa(None, 32, 48, 4096, 8192, 1, 8, 2, 8, 64, 0, 0.125, None) == -1
     assert lib.fa_fwd_gqa(*base, 1, 8, 2, 8, 96, 0, 0.125, None) == -3
+
+
+def test_decode_argument_checks(lib):
+    need = lib.fa_decode_workspace_bytes(2, 8, 2, 1000, 128)
+    assert need > 0 and need % 256 == 0
+    assert lib.fa_decode_workspace_bytes(2, 12, 1, 1000, 128) == 0  # group 12 unsupported
+    assert lib.fa_decode_workspace_bytes(2, 8, 3, 1000, 128) == 0   # 3 does not divide 8
+    ws = 1 << 24
+    args = (16, 1 << 20, 2 << 20, 4096, 8192)
+    assert lib.fa_decode(*args, ws, need, 2, 12, 1, 1000, 128, 0.1, None) == -8
+    assert lib.fa_decode(*args, ws, need, 2, 8, 2, 1000, 96, 0.1, None) == -3
+    assert lib.fa_decode(*args, None, need, 2, 8, 2, 1000, 128, 0.1, None) == -11
+    assert lib.fa_decode(*args, ws, need - 1, 2, 8, 2, 1000, 128, 0.1, None) == -11
+    assert lib.fa_decode(*args, ws + 16, need, 2, 8, 2, 1000, 128, 0.1, None) == -11
+    assert lib.fa_decode(None, 1 << 20, 2 << 20, 4096, 8192, ws, need, 2, 8, 2, 1000, 128,
+                         0.1, None) == -1
+    assert lib.fa_decode(*args, ws, need, 2, 8, 2, 1000, 128, 0.0, None) == -9

@@ -338,3 +338,37 @@ def test_gqa_reduces_to_mha_and_mqa():
         np.testing.assert_array_equal(Lm[:, h:h + 1], Lh)
     with pytest.raises(ValueError):
         oracle.attention_fwd_gqa(q, k[:, :3], v[:, :3])
+
+
+# ------------------------------------------ decoding (query rows at the end)
+def test_decode_rows_are_the_last_rows_of_causal_attention():
+    """The newest Nq query rows against the whole cache equal the last Nq
+    rows of causal self-attention over the full sequence."""
+    rng = np.random.default_rng(32)
+    B, H, H_kv, N, d = 2, 4, 2, 37, 8
+    q_all = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, H_kv, N, d))
+    v = rng.standard_normal((B, H_kv, N, d))
+    O_all, L_all = oracle.attention_fwd_gqa(q_all, k, v, causal=True, scale=0.4)
+    for Nq in (1, 3, N):
+        O, L = oracle.attention_decode(q_all[:, :, N - Nq:], k, v, causal=True, scale=0.4)
+        np.testing.assert_allclose(O, O_all[:, :, N - Nq:], atol=1e-13)
+        np.testing.assert_allclose(L, L_all[:, :, N - Nq:], atol=1e-13)
+
+
+def test_decode_single_row_closed_forms():
+    rng = np.random.default_rng(33)
+    B, H, N, d = 1, 2, 29, 6
+    q = rng.standard_normal((B, H, 1, d))
+    k = np.broadcast_to(rng.standard_normal((B, H, 1, d)), (B, H, N, d)).copy()
+    v = rng.standard_normal((B, H, N, d))
+    O, L = oracle.attention_decode(q, k, v, scale=0.5)
+    np.testing.assert_allclose(O[:, :, 0], v.mean(axis=2), atol=1e-13)
+    s = 0.5 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0])
+    np.testing.assert_allclose(L[:, :, 0], s + math.log(N), atol=1e-12)
+    # brute force for one row (random keys) in 40-digit decimals
+    kr = rng.standard_normal((N, d))
+    Ob, Lb = _brute(np.concatenate([np.zeros((N - 1, d)), q[0, 0]]), kr, v[0, 0], True, 0.5)
+    Od, Ld = oracle.attention_decode(q[:1, :1], kr[None, None], v[:1, :1], scale=0.5)
+    np.testing.assert_allclose(Od[0, 0, 0], Ob[-1], atol=1e-13)
+    assert abs(Ld[0, 0, 0] - Lb[-1]) < 1e-13

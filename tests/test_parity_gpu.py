@@ -244,3 +244,53 @@ def test_llama_gqa_workload_sampled(fa):
     o = o_d.float()[0].cpu().numpy()
     lse = lse_d[0].cpu().numpy()
     check(o[idx, rows][None], lse[idx, rows][None], O_ref, L_ref, "llama_gqa")
+
+
+# ------------------------------------------------------------ decoding
+from online_softmax_fa_gb300.inputs import DECODE_WORKLOADS, make_decode  # noqa: E402
+
+
+def _decode_check(fa, q, k, v, scale, what):
+    dev = torch.device("cuda")
+    o, lse = fa.fa_decode(q.to(dev), k.to(dev), v.to(dev), scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    O_ref, L_ref = oracle.attention_decode(q.unsqueeze(2), k, v, scale=scale)
+    return check(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref[:, :, 0], L_ref[:, :, 0],
+                 what)
+
+
+@pytest.mark.parametrize("N", [1, 7, 63, 64, 65, 1000, 4097])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,H_kv", [(8, 8), (8, 4), (8, 2), (8, 1)])
+def test_decode_parity(fa, N, d, H, H_kv):
+    q, k, v = make_decode(2, H, H_kv, N, d, seed=60 + N + H_kv)
+    _decode_check(fa, q, k, v, scale_of(d), f"decode N={N} d={d} H={H} H_kv={H_kv}")
+
+
+def test_decode_closed_form_identical_keys(fa):
+    q, k, v = make_decode(1, 4, 2, 3000, 128, seed=70)
+    k = k[:, :, :1].expand(-1, -1, 3000, -1).contiguous()
+    dev = torch.device("cuda")
+    o, lse = fa.fa_decode(q.to(dev), k.to(dev), v.to(dev), scale=0.1)
+    torch.cuda.synchronize()
+    mean_v = v.double().mean(dim=2).repeat_interleave(2, dim=1).numpy()
+    assert np.abs(o.float().cpu().numpy() - mean_v).max() <= O_MAX
+
+
+def test_decode_workload(fa):
+    w = DECODE_WORKLOADS["decode"]
+    q, k, v = make_decode(w.B, w.H, w.kv_heads, w.N, w.d, w.seed)
+    _decode_check(fa, q, k, v, w.scale, "decode workload")
+
+
+def test_decode_matches_forward_last_row(fa):
+    """The newest row decoded against the cache equals the last row of the
+    causal forward pass over the whole sequence."""
+    q, k, v = make_qkv(1, 8, 777, 128, seed=71, H_kv=2)
+    dev = torch.device("cuda")
+    o_f, l_f = fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    o_d, l_d = fa.fa_decode(q[:, :, -1].contiguous().to(dev), k.to(dev), v.to(dev))
+    torch.cuda.synchronize()
+    assert (o_f[:, :, -1].float() - o_d.float()).abs().max().item() <= 2 * O_MAX
+    assert (l_f[:, :, -1] - l_d).abs().max().item() <= 2 * LSE_MAX
