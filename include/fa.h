@@ -152,6 +152,31 @@ int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
               int N, int d, float scale, fa_stream_t stream);
 
 /*
+ * fa_decode_noalloc -- fa_decode for callers that cannot allocate device
+ * memory when they decode (an allocation can block on or synchronise with
+ * queued device work, can fail once a host framework's pool owns the free
+ * memory, and some plugin hosts give a component only its input and output
+ * buffers).  The pages have no counterpart: this is an interface variant.
+ * Same arguments as fa_decode minus the workspace: the split states live in
+ * a 16 MiB area of device memory that the library owns (every GPU that
+ * loads the library keeps it reserved until the process exits).
+ *   - Requests whose states need more than 16 MiB, i.e.
+ *     fa_decode_workspace_bytes(B, H, H_kv, N, d) > 16 MiB, return
+ *     FA_ERR_WORKSPACE (fa_last_error_detail says why) and enqueue nothing.
+ *   - Allocates nothing, on the host or the device.
+ *   - The first call on each device looks up the area's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call shares the one area: calls that overlap on the GPU (other
+ *     streams, other host threads) race and must be ordered by the caller.
+ *     Nothing in it has to start at zero: each call writes every state it
+ *     later reads.
+ */
+int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                      int B, int H, int H_kv, int N, int d, float scale,
+                      fa_stream_t stream);
+
+/*
  * fa_device_error -- synchronises `stream`, then reads and clears the
  * library's device status word on the current device.  Returns FA_OK, or
  * FA_ERR_TIMEOUT if a kernel since the last call gave up on a bounded wait

@@ -269,6 +269,27 @@ int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
     return fa::launch_decode(a);
 }
 
+int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
+                      int H, int H_kv, int N, int d, float scale, fa_stream_t stream) {
+    if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
+    int rc = check_decode_shape(B, H, H_kv, N, d, scale);
+    if (rc != FA_OK) return rc;
+    size_t acc_bytes = 0, ml_bytes = 0;
+    decode_layout(B, H, H_kv, N, d, &acc_bytes, &ml_bytes);
+    if (acc_bytes + ml_bytes > (static_cast<size_t>(16) << 20))
+        return fa::record_message(FA_ERR_WORKSPACE,
+                                  "request needs more than the 16 MiB of library-owned "
+                                  "decoding scratch; use fa_decode with a workspace");
+    rc = check_arch();
+    if (rc != FA_OK) return rc;
+    void *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    rc = fa::decode_static_scratch(&scratch, &scratch_bytes);
+    if (rc != FA_OK) return rc;
+    // Same checks and kernels as the caller-workspace entry point.
+    return fa_decode(Q, K, V, O, LSE, scratch, scratch_bytes, B, H, H_kv, N, d, scale, stream);
+}
+
 int fa_device_error(fa_stream_t stream) {
     int v = 0;
     const int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);

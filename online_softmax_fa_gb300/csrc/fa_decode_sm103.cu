@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "fa_internal.h"
 
@@ -295,6 +296,49 @@ int launch_decode(const DecodeArgs &a) {
     if (a.d == 64) return launch_decode_d<64>(a);
     if (a.d == 128) return launch_decode_d<128>(a);
     return FA_ERR_HEADDIM;
+}
+
+}  // namespace fa
+
+// ----------------------------------------------------- no-allocation decoding
+// fa_decode_noalloc() runs the same two kernels as fa_decode() but keeps the
+// split states in a fixed area of device memory that the library itself
+// owns, so the caller never has to allocate.  That is for callers that
+// cannot call cudaMalloc at the point where they decode: an allocation can
+// block on, or synchronise with, work already queued on the device, it can
+// fail once a host framework's memory pool has claimed the free memory, and
+// some plugin hosts hand a component only the buffers of its inputs and
+// outputs.
+//
+// The area is 16 MiB; every GPU that loads this library keeps it reserved
+// until the process exits.  Requests whose states need more are rejected.
+namespace fa {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64] = {nullptr};
+}  // namespace
+
+// Device address of g_decode_scratch on the current device.  In host code
+// the symbol names a host-side stand-in, not device memory, so the address
+// is asked for once per device, with that device current, and cached.
+int decode_static_scratch(void **ptr, size_t *bytes) {
+    int dev = 0;
+    FA_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return record_message(FA_ERR_ARCH, "device ordinal out of range");
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        FA_CUDA_TRY(cudaGetSymbolAddress(&p, g_decode_scratch));
+        g_scratch_addr[dev] = p;
+    }
+    *ptr = g_scratch_addr[dev];
+    *bytes = kNoAllocScratchBytes;
+    return FA_OK;
 }
 
 }  // namespace fa

@@ -38,6 +38,9 @@ struct DecodeArgs {
 };
 int launch_decode(const DecodeArgs &a);
 int decode_n_splits(int B, int H_kv, int N);
+// Device address and size of the library-owned scratch area that
+// fa_decode_noalloc uses (resolved once per device).
+int decode_static_scratch(void **ptr, size_t *bytes);
 
 // Records the CUDA error of a failed call (thread-local) for
 // fa_last_error_detail(); returns FA_ERR_LAUNCH.
