@@ -52,6 +52,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_decode_workspace_bytes.restype = S
     lib.fa_decode.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
     lib.fa_decode.restype = I
+    lib.fa_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
+    lib.fa_decode_noalloc.restype = I
     lib.fa_device_error.argtypes = [P]
     lib.fa_device_error.restype = I
     lib.fa_selftest_bounded_wait.argtypes = [I, P]
