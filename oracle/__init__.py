@@ -61,6 +61,9 @@ def _load():
                                         ctypes.c_int, ctypes.c_double, p, i64,
                                         ctypes.c_int]
         lib.fa_oracle_fwd_q.restype = ctypes.c_int
+        lib.fa_oracle_bwd.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_int]
+        lib.fa_oracle_bwd.restype = ctypes.c_int
         lib.fa_oracle_fwd_blockwise.argtypes = [
             p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
             p, i64, p, i64, ctypes.c_int, p, p, p, ctypes.c_int]
@@ -196,6 +199,33 @@ def attention_decode(q, k, v, causal: bool = True, scale: float | None = None,
     if rc != 0:
         raise ValueError(f"fa_oracle_fwd_q failed ({rc})")
     return O.reshape(B, H, Nq, dv), LSE.reshape(B, H, Nq)
+
+
+def attention_bwd(q, k, v, do, causal: bool = False, scale: float | None = None,
+                  nthreads: int | None = None, return_D: bool = False):
+    """Gradients (dQ, dK, dV) of the forward pass for the output gradient
+    dO, by the definition (fp64, S, P, dP, dS materialised per head).
+    q, k, v, do: [..., N, d].  With ``return_D`` also D_i = sum_r dO_ir O_ir."""
+    q, k, v, do = (_as_f64(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")))
+    if not (q.shape == k.shape == v.shape == do.shape) or q.ndim < 2:
+        raise ValueError("q, k, v, do must share one shape [..., N, d]")
+    lead = q.shape[:-2]
+    N, d = q.shape[-2], q.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = (np.empty((BH, N, d)) for _ in range(3))
+    D = np.empty((BH, N))
+    q, k, v, do = (np.ascontiguousarray(x) for x in (q, k, v, do))
+    rc = _load().fa_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(D), BH, N, d, 1 if causal else 0,
+                               float(scale), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"fa_oracle_bwd failed ({rc})")
+    out = (dq.reshape(q.shape), dk.reshape(q.shape), dv.reshape(q.shape))
+    if return_D:
+        out = out + (D.reshape(*lead, N),)
+    return out
 
 
 def attention_fwd_blockwise(q, k, v, bounds, causal: bool = False,

@@ -329,3 +329,128 @@ int fa_oracle_fwd_blockwise(const double *Q, const double *K, const double *V,
     jb.M_out = M_out; jb.L_out = L_out; jb.A_out = A_out;
     return run_threads(&jb, blockwise_worker, nthreads);
 }
+
+/*
+ * fa_oracle_bwd -- gradients of the attention forward pass, by the plain
+ * definition ("Understanding FlashAttention Pt 1", section 3.6 "Backward
+ * Pass: Recompute Instead of Save"), materialised in fp64 per (b, h):
+ *   S = scale * Q K^T (causal: S_ij = -inf for j > i), P = softmax_rows(S),
+ *   O = P V, dV = P^T dO, dP = dO V^T, D_i = sum_r dO_ir O_ir,
+ *   dS = P * (dP - D_i), dQ = scale * dS K, dK = scale * dS^T Q.
+ * O is recomputed here from Q, K, V (not taken from the caller).
+ * Layouts: Q, K, V, dO, dQ, dK, dV are [BH, N, d] fp64; D_out (optional,
+ * may be NULL) is [BH, N].  Returns 0, -1 (bad argument) or -2 (memory).
+ */
+typedef struct {
+    const double *Q, *K, *V, *dO;
+    double *dQ, *dK, *dV, *D_out;
+    int64_t BH, N, d;
+    int causal;
+    double scale;
+    int64_t next;
+    int failed;
+} bwd_job;
+
+static void bwd_head(bwd_job *jb, int64_t bh, double *S, double *P, double *dP) {
+    const int64_t N = jb->N, d = jb->d;
+    const double *Q = jb->Q + bh * N * d, *K = jb->K + bh * N * d, *V = jb->V + bh * N * d;
+    const double *dO = jb->dO + bh * N * d;
+    double *dQ = jb->dQ + bh * N * d, *dK = jb->dK + bh * N * d, *dV = jb->dV + bh * N * d;
+    /* forward: S, P (row softmax), O = P V is folded into D below */
+    for (int64_t i = 0; i < N; ++i) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += Q[i * d + c] * K[j * d + c];
+            S[i * N + j] = (jb->causal && j > i) ? -INFINITY : jb->scale * dot;
+            if (S[i * N + j] > m) m = S[i * N + j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            P[i * N + j] = (m == -INFINITY) ? 0.0 : exp(S[i * N + j] - m);
+            l += P[i * N + j];
+        }
+        for (int64_t j = 0; j < N; ++j) P[i * N + j] = (l > 0.0) ? P[i * N + j] / l : 0.0;
+    }
+    /* dP = dO V^T */
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += dO[i * d + c] * V[j * d + c];
+            dP[i * N + j] = dot;
+        }
+    /* D_i = sum_r dO_ir O_ir with O = P V */
+    for (int64_t i = 0; i < N; ++i) {
+        double Di = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            double o = 0.0;
+            for (int64_t j = 0; j < N; ++j) o += P[i * N + j] * V[j * d + c];
+            Di += dO[i * d + c] * o;
+        }
+        if (jb->D_out) jb->D_out[bh * N + i] = Di;
+        /* dS overwrites dP */
+        for (int64_t j = 0; j < N; ++j) dP[i * N + j] = P[i * N + j] * (dP[i * N + j] - Di);
+    }
+    /* dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K */
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t c = 0; c < d; ++c) {
+            double v = 0.0, k = 0.0;
+            for (int64_t i = 0; i < N; ++i) {
+                v += P[i * N + j] * dO[i * d + c];
+                k += dP[i * N + j] * Q[i * d + c];
+            }
+            dV[j * d + c] = v;
+            dK[j * d + c] = jb->scale * k;
+        }
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t c = 0; c < d; ++c) {
+            double q = 0.0;
+            for (int64_t j = 0; j < N; ++j) q += dP[i * N + j] * K[j * d + c];
+            dQ[i * d + c] = jb->scale * q;
+        }
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_job *jb = (bwd_job *)arg;
+    const size_t nn = (size_t)jb->N * (size_t)jb->N;
+    double *S = (double *)malloc(sizeof(double) * nn);
+    double *P = (double *)malloc(sizeof(double) * nn);
+    double *dP = (double *)malloc(sizeof(double) * nn);
+    if (!S || !P || !dP) {
+        __atomic_store_n(&jb->failed, 1, __ATOMIC_SEQ_CST);
+    } else {
+        for (;;) {
+            const int64_t bh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_SEQ_CST);
+            if (bh >= jb->BH) break;
+            bwd_head(jb, bh, S, P, dP);
+        }
+    }
+    free(S);
+    free(P);
+    free(dP);
+    return NULL;
+}
+
+int fa_oracle_bwd(const double *Q, const double *K, const double *V, const double *dO,
+                  double *dQ, double *dK, double *dV, double *D_out, int64_t BH, int64_t N,
+                  int64_t d, int causal, double scale, int nthreads) {
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return -1;
+    if (BH < 1 || N < 1 || d < 1) return -1;
+    bwd_job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.Q = Q; jb.K = K; jb.V = V; jb.dO = dO;
+    jb.dQ = dQ; jb.dK = dK; jb.dV = dV; jb.D_out = D_out;
+    jb.BH = BH; jb.N = N; jb.d = d; jb.causal = causal ? 1 : 0; jb.scale = scale;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > BH) nthreads = (int)BH;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t tid[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, bwd_worker, &jb) != 0) break;
+        ++started;
+    }
+    if (started == 0) bwd_worker(&jb);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    return jb.failed ? -2 : 0;
+}

@@ -372,3 +372,53 @@ def test_decode_single_row_closed_forms():
     Od, Ld = oracle.attention_decode(q[:1, :1], kr[None, None], v[:1, :1], scale=0.5)
     np.testing.assert_allclose(Od[0, 0, 0], Ob[-1], atol=1e-13)
     assert abs(Ld[0, 0, 0] - Lb[-1]) < 1e-13
+
+
+# ------------------------------------------------------------------ backward
+def _loss(q, k, v, do, causal, scale):
+    O, _ = oracle.attention_fwd(q, k, v, causal=causal, scale=scale)
+    return float(np.sum(O * do))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    """d(sum O * dO)/dX by central differences (the definition of the
+    gradient) for every element of Q, K, V on a tiny head."""
+    rng = np.random.default_rng(40 + causal)
+    N, d, scale = 6, 3, 0.7
+    q, k, v, do = (rng.standard_normal((1, N, d)) for _ in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale)
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            x0 = x[idx]
+            x[idx] = x0 + eps
+            fp = _loss(q, k, v, do, causal, scale)
+            x[idx] = x0 - eps
+            fm = _loss(q, k, v, do, causal, scale)
+            x[idx] = x0
+            num[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(g, num, atol=1e-7, rtol=1e-6)
+
+
+def test_backward_identities():
+    """Rows of dS sum to zero, so shifting every key by u leaves dQ unchanged
+    and every key-gradient sum is zero; D_i = sum_r dO_ir O_ir."""
+    rng = np.random.default_rng(42)
+    q, k, v, do = (rng.standard_normal((2, 40, 8)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv, D = oracle.attention_bwd(q, k, v, do, causal=causal, scale=0.3,
+                                             return_D=True)
+        O, _ = oracle.attention_fwd(q, k, v, causal=causal, scale=0.3)
+        np.testing.assert_allclose(D, np.sum(do * O, axis=-1), atol=1e-12)
+        # sum_j dK_j = scale * sum_i (sum_j dS_ij) q_i = 0
+        np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+        dq2, _, dv2 = oracle.attention_bwd(q, k + rng.standard_normal(8), v, do,
+                                           causal=causal, scale=0.3)
+        np.testing.assert_allclose(dq2, dq, atol=1e-11)
+        np.testing.assert_allclose(dv2, dv, atol=1e-11)
+        # dV = P^T dO: with dO = all ones, the column sums of P (keys' total weight)
+        _, _, dv1 = oracle.attention_bwd(q, k, v, np.ones_like(do), causal=causal, scale=0.3)
+        if not causal:
+            np.testing.assert_allclose(dv1.sum(axis=1), 40.0 * np.ones((2, 8)), atol=1e-10)
