@@ -435,6 +435,64 @@ def run_decode(args, w):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------- backward leg
+def run_backward(args, w, causal):
+    """fa_bwd on the workload: TFLOP/s over the nominal backward FLOPs,
+    10*B*H*N^2*d (five N x N x d products: S, dP, dV, dK, dQ), halved when
+    causal.  The kernels recompute S and dP once more for dQ (seven
+    products); the metric counts the nominal five."""
+    import torch
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from online_softmax_fa_gb300 import fa
+    from online_softmax_fa_gb300.build import build_library
+    from online_softmax_fa_gb300.inputs import make_grad
+    build_library()
+    fa.load_library()
+    q, k, v = make_workload(w)
+    do = make_grad(w.B, w.H, w.N, w.d, w.seed)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=w.scale)
+    grads = [tuple(torch.empty_like(qd) for _ in range(3)) for _ in range(2)]
+    wsb = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                      device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        dq, dk, dv = grads[i % 2]
+        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws_)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        dq, dk, dv = grads[i % 2]
+        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_)
+    if fa.fa_device_error() != 0:
+        raise RuntimeError("device status set during the backward leg")
+    ms = max_over_ranks(e0.elapsed_time(e1), ws_) / args.steps
+    if rank != 0:
+        return
+    flops = 2.5 * w.flops(causal)
+    peak, _, peak_kind = load_peaks()
+    value = ws_ * flops / (ms * 1e-3) / 1e12
+    out = {"metric": "attn bwd TFLOP/s (10·B·H·N²·d, causal halved)", "value": value,
+           "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": workload_config(w, causal),
+           "roofline": {"bound": "tensor", "achieved": value / ws_, "peak": peak,
+                        "unit": "TFLOP/s", "frac": value / ws_ / peak,
+                        "peak_source": f"bf16_tflops (burst) of {peak_kind}",
+                        "traffic": None, "kernel": "pre + dkdv + dq (three launches)"},
+           "gpu_launches": 3 * args.steps}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,6 +503,8 @@ def main(argv=None):
                     default="llama")
     ap.add_argument("--causal", choices=["auto", "0", "1"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time fa_bwd (gradients) instead of the forward pass")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -464,7 +524,9 @@ def main(argv=None):
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     try:
-        if args.impl == "reference":
+        if args.backward:
+            run_backward(args, w, causal)
+        elif args.impl == "reference":
             run_reference(args, w, causal)
         else:
             run_ours(args, w, causal)

@@ -119,6 +119,37 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host,
                 int causal, float scale, fa_stream_t stream);
 
 /*
+ * fa_bwd_workspace_bytes -- device workspace fa_bwd needs: one fp32 per
+ * query row (D_i = sum_r dO_ir O_ir), 256-byte aligned.  0 if invalid.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_bwd -- gradients of fa_fwd by recomputation ("Understanding
+ * FlashAttention Pt 1", section 3.6): the probability tiles are rebuilt from
+ * the forward's LSE (P_ij = exp(S_ij - LSE_i), "Fix 2" of "FlashAttention-2
+ * -- Deeper Math") instead of being stored, and
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_r dO_ir O_ir,
+ *   dS = P * (dP - D_i),  dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ *   Q, K, V, O, dO  bf16 [B, H, N, d] (O and LSE as fa_fwd wrote them for
+ *                   the same Q, K, V, causal and scale), device, read
+ *   LSE             fp32 [B, H, N], device, read
+ *   dQ, dK, dV      bf16 [B, H, N, d], device, written
+ *   workspace       caller-owned device scratch of at least
+ *                   fa_bwd_workspace_bytes(B, H, N, d) bytes, 256-byte aligned
+ * Three kernels on `stream` (D, then dK/dV with key blocks outermost, then
+ * dQ with query blocks outermost); no atomics, so the result is
+ * deterministic.  Checks and errors as fa_fwd (outputs and workspace must
+ * not overlap any input or each other; FA_ERR_WORKSPACE for a missing,
+ * small or misaligned workspace).
+ */
+int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+           const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
+           size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
  * fa_decode_workspace_bytes -- device workspace fa_decode needs: the
  * per-split softmax states (m, l and the d-wide accumulator for every
  * query head and key split).  Returns 0 for an invalid or unsupported shape.

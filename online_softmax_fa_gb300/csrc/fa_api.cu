@@ -290,11 +290,75 @@ int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, floa
     return fa_decode(Q, K, V, O, LSE, scratch, scratch_bytes, B, H, H_kv, N, d, scale, stream);
 }
 
-int fa_device_error(fa_stream_t stream) {
-    int v = 0;
-    const int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
+// ------------------------------------------------------------ backward
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
+    return align256(static_cast<size_t>(B) * H * N * sizeof(float));
+}
+
+int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+           const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
+           size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
+           fa_stream_t stream) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_NULL;
+    int rc = check_shape(B, H, N, d, scale);
     if (rc != FA_OK) return rc;
-    return v == 0 ? FA_OK : FA_ERR_TIMEOUT;
+    const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (mis16(Q) || mis16(K) || mis16(V) || mis16(O) || mis16(dO) || mis16(dQ) || mis16(dK) ||
+        mis16(dV) || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
+        return FA_ERR_ALIGN;
+    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_WORKSPACE;
+    const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
+    const struct { const void *p; size_t n; } ins[] = {
+        {Q, t_bytes}, {K, t_bytes}, {V, t_bytes}, {O, t_bytes}, {dO, t_bytes}, {LSE, l_bytes}};
+    const struct { const void *p; size_t n; } outs[] = {
+        {dQ, t_bytes}, {dK, t_bytes}, {dV, t_bytes}, {workspace, need}};
+    for (const auto &o : outs) {
+        for (const auto &in : ins)
+            if (overlaps(o.p, o.n, in.p, in.n)) return FA_ERR_ALIAS;
+        for (const auto &o2 : outs)
+            if (&o2 != &o && overlaps(o.p, o.n, o2.p, o2.n)) return FA_ERR_ALIAS;
+    }
+    rc = check_arch();
+    if (rc != FA_OK) return rc;
+    CUtensorMap tmQ, tmK, tmV, tmdO;
+    const int BH = B * H;
+    if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, BH, N, d) ||
+        !encode_qkv_map(&tmV, V, BH, N, d) || !encode_qkv_map(&tmdO, dO, BH, N, d))
+        return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    fa::BwdArgs a;
+    a.tmQ = &tmQ;
+    a.tmK = &tmK;
+    a.tmV = &tmV;
+    a.tmdO = &tmdO;
+    a.O = O;
+    a.dO = dO;
+    a.LSE = LSE;
+    a.Dvec = static_cast<float *>(workspace);
+    a.dQ = dQ;
+    a.dK = dK;
+    a.dV = dV;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.causal = causal != 0;
+    a.scale = scale;
+    a.limit_ns = kWaitLimitNs;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return fa::launch_bwd(a);
+}
+
+int fa_device_error(fa_stream_t stream) {
+    int v = 0, vb = 0;
+    int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
+    if (rc != FA_OK) return rc;
+    rc = fa::bwd_read_and_clear_status(&vb);
+    if (rc != FA_OK) return rc;
+    return (v == 0 && vb == 0) ? FA_OK : FA_ERR_TIMEOUT;
 }
 
 int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {

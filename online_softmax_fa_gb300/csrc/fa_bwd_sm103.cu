@@ -1,0 +1,569 @@
+// fa_bwd_sm103.cu -- attention backward pass for sm_103a (GB300).
+//
+// Gradients of O = softmax(scale * Q K^T [+causal]) V for an output gradient
+// dO, by recomputation ("Understanding FlashAttention Pt 1", wpnews.pro,
+// section 3.6 "Backward Pass: Recompute Instead of Save"): the probability
+// tiles are rebuilt from the saved per-row LSE ("Fix 2" of "FlashAttention-2
+// -- Deeper Math": P_ij = exp(S_ij - L_i)) instead of being stored, and
+//   dV += P^T dO,  dP = dO V^T,  dS = P * (dP - D_i),
+//   dQ += scale * dS K,  dK += scale * dS^T Q,
+// with D_i = sum_r dO_ir O_ir.
+//
+// Three kernels, all deterministic (no atomics, fixed summation order):
+//   * pre:  D = rowsum(dO * O) in fp32, one warp per row.
+//   * dkdv: one CTA per (b, h, 128-key block j), query blocks i as the inner
+//           loop.  On tcgen05 with TMEM accumulators: S^T = K_j Q_i^T and
+//           dP^T = V_j dO_i^T (keys are the MMA rows), then four elementwise
+//           warps (thread = key row = TMEM lane) form P^T and dS^T in bf16
+//           over the S^T / dP^T columns, then dV_j += P^T dO_i and
+//           dK_j += dS^T Q_i read them from TMEM.
+//   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
+//           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
+//           then dQ_i += dS K_j.
+// Causal: blocks entirely above the diagonal are skipped; the diagonal block
+// is masked.  TMEM (dkdv): S^T [0,128), dP^T [128,256), dV [256,256+d),
+// dK [256+d, 256+2d); P^T and dS^T are bf16 over the first 64 columns of
+// S^T and dP^T.  TMEM (dq): S [0,128), dP [128,256), dQ [256,256+d).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "sm103_primitives.cuh"
+
+namespace fa {
+
+// Device status word of the backward kernels (read with the forward's by
+// fa_device_error): 0 or the site of the first bounded wait that expired.
+__device__ int g_fa_status_bwd;
+
+namespace bwd {
+
+constexpr int kBlk = 128;             // rows per block (keys or queries)
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+constexpr int kThreads = 192;         // 4 elementwise warps + MMA + TMA
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int { kSiteKV = 0x21, kSiteQ, kSiteS, kSiteP, kSiteO, kSiteEmpty };
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTile = kChunks * kBoxBytes;  // one [128 x D] bf16 tile
+    static constexpr int kStages = 2;
+    // dkdv: K_j, V_j once; Q_i, dO_i per stage; LSE2 and D per stage (floats)
+    static constexpr int kOffA = 0;                 // K_j (dkdv) / Q_i (dq)
+    static constexpr int kOffB = kTile;             // V_j (dkdv) / dO_i (dq)
+    static constexpr int kOffRing = 2 * kTile;      // stages of two tiles each
+    static constexpr int kOffRows = kOffRing + kStages * 2 * kTile;  // LSE2, D per stage
+    static constexpr int kOffBar = kOffRows + kStages * 2 * kBlk * 4;
+    static constexpr int kNumBars = 1 + 2 * kStages + 3;  // once, full/empty[S], s, p, o
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr uint32_t kTmS = 0, kTmP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(kBlk, kBlk, false);
+    static constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBlk, D, true);
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Params {
+    __nv_bfloat16 *g0, *g1;  // dkdv: dK, dV; dq: dQ
+    const float *LSE, *Dvec;
+    int N, BH, n_blocks;
+    float scale, scale_log2;
+    uint64_t limit_ns;
+};
+
+template <int D>
+struct View {
+    uint8_t *a, *b, *ring;
+    float *rows;
+    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;
+    uint32_t *tmem_slot;
+    volatile int *abort_flag;
+};
+
+template <int D>
+__device__ __forceinline__ View<D> view() {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    View<D> v;
+    v.a = smem + C::kOffA;
+    v.b = smem + C::kOffB;
+    v.ring = smem + C::kOffRing;
+    v.rows = reinterpret_cast<float *>(smem + C::kOffRows);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    v.once = bar;
+    v.full = bar + 1;
+    v.empty = v.full + C::kStages;
+    v.s_full = v.empty + C::kStages;
+    v.p_full = v.s_full + 1;
+    v.o_full = v.p_full + 1;
+    v.tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    v.abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    return v;
+}
+
+// M128 x N128 x K(D) with both operands K-major [rows x D] in swizzled chunks.
+template <int D>
+__device__ __forceinline__ void mma_rows_rows(uint32_t d_tm, uint64_t da, uint64_t db) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+        mma_ss_elect(d_tm, da + off, db + off, Cfg<D>::kIdescS, kk > 0 ? 1u : 0u);
+    }
+}
+
+// acc[M128 x N(D)] (+)= A[tmem, 128 x 128 bf16] * B[128 rows x D, MN-major].
+template <int D>
+__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tm, uint32_t a_tm, uint64_t db, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 16; ++kk)
+        mma_ts_elect(d_tm, a_tm + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                     Cfg<D>::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, uint64_t *bar,
+                                          int row, int bh, uint64_t pol) {
+#pragma unroll
+    for (int c = 0; c < Cfg<D>::kChunks; ++c)
+        tma_load_3d(dst + c * kBoxBytes, m, bar, 64 * c, row, bh, pol);
+}
+
+__device__ __forceinline__ void setup_barriers(uint64_t *once, uint64_t *full, uint64_t *empty,
+                                               uint64_t *s_full, uint64_t *p_full,
+                                               uint64_t *o_full, volatile int *abort_flag,
+                                               int stages) {
+    mbar_init(once, 1);
+    for (int s = 0; s < stages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_full, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+}
+
+// Elementwise part shared by both kernels: for 32 consecutive columns,
+// p = 2^(s*c - lse2) (0 where masked), ds = p * (dp - D); returns packed bf16
+// p and ds.  lse2/dd give the per-column (dkdv) or per-row (dq) statistics.
+__device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                           const float *lse2, const float *dd, bool col_stats,
+                                           float my_lse2, float my_d, float cs, int lim_lo,
+                                           int lim_hi, int col0, uint32_t (&pp)[16],
+                                           uint32_t (&pds)[16]) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        float p[2], ds[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = 2 * t + u;
+            const int col = col0 + e;
+            const float l2 = col_stats ? lse2[e] : my_lse2;
+            const float dv = col_stats ? dd[e] : my_d;
+            const bool keep = col >= lim_lo && col < lim_hi;
+            p[u] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), cs, -l2)) : 0.f;
+            ds[u] = p[u] * (__uint_as_float(dp[e]) - dv);
+        }
+        pp[t] = pack_bf16x2(p[0], p[1]);
+        pds[t] = pack_bf16x2(ds[0], ds[1]);
+    }
+}
+
+// ============================== dK / dV kernel ==============================
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const Params p) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.n_blocks;
+    const int jb = blockIdx.x % p.n_blocks;  // key block
+    const int N = p.N;
+    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
+    const int n_q = p.n_blocks - i0;
+    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
+                                         v.abort_flag, C::kStages);
+    if (warp == kMmaWarp) {
+        tmem_alloc(v.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+
+    if (warp == kTmaWarp) {
+        // ---- producer: K_j, V_j once; per query block Q_i, dO_i (TMA) and
+        // LSE2_i, D_i (plain loads by the whole warp, bounds-checked)
+        const uint64_t pol = l2_policy_evict_last();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(v.once, 2 * C::kTile);
+            load_tile<D>(v.a, &tmK, v.once, jb * kBlk, bh, pol);
+            load_tile<D>(v.b, &tmV, v.once, jb * kBlk, bh, pol);
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < n_q && ok; ++t) {
+            const int s = t % C::kStages;
+            if (t >= C::kStages)
+                ok = __all_sync(0xffffffffu, mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1,
+                                                       ctl, kSiteEmpty));
+            if (!ok) break;
+            const int q0 = (i0 + t) * kBlk;
+            float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
+            for (int e = lane; e < kBlk; e += 32) {
+                const int q = q0 + e;
+                const bool in = q < N;
+                lse2[e] = in ? p.LSE[static_cast<size_t>(bh) * N + q] * kLog2e : 0.f;
+                dd[e] = in ? p.Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                uint8_t *st = v.ring + s * 2 * C::kTile;
+                mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
+                load_tile<D>(st, &tmQ, &v.full[s], q0, bh, pol);
+                load_tile<D>(st + C::kTile, &tmdO, &v.full[s], q0, bh, pol);
+            }
+            ++issued;
+        }
+        if (lane == 0) {  // drain the loads in flight
+            mbar_wait_drain(v.once, 0, p.limit_ns);
+            for (int t = max(0, issued - C::kStages); t < issued; ++t)
+                mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---- MMA issuer (converged warp, elected lane)
+        const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
+        const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
+        const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
+        const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
+        const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+        };
+        bool ok = wait(v.once, 0, kSiteKV);
+        if (ok) tc_fence_after();
+        for (int t = 0; t < n_q && ok; ++t) {
+            const int s = t % C::kStages;
+            ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
+            const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+            mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so);        // S^T = K Q^T
+            mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so + to);   // dP^T = V dO^T
+            mma_commit_elect(v.s_full);
+            ok = wait(v.p_full, t & 1, kSiteP);
+            if (!ok) break;
+            tc_fence_after();
+            mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0);  // dV
+            mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmP, ring_mn + so, t > 0);       // dK
+            mma_commit_elect(&v.empty[s]);
+        }
+        mma_commit_elect(v.o_full);
+        mbar_wait_drain(v.o_full, 0, p.limit_ns);
+    } else {
+        // ---- elementwise: thread = key row r of this block
+        const int row = warp * 32 + lane;
+        const int key = jb * kBlk + row;
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        bool ok = true;
+        for (int t = 0; t < n_q && ok; ++t) {
+            const int s = t % C::kStages;
+            ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+            // the producer's LSE/D rows of this stage: observe them directly
+            // (the stage cannot be refilled before this block's p_full)
+            if (ok) ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
+            if (!ok) break;
+            tc_fence_after();
+            const int q0 = (i0 + t) * kBlk;
+            const float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
+            // column (query) q kept iff q < N and, causal, q >= key
+            const int lim_lo = CAUSAL ? key - q0 : 0;
+            const int lim_hi = N - q0;
+#pragma unroll 1
+            for (int c = 0; c < kBlk / 32; ++c) {
+                uint32_t sv[32], dp[32], pp[16], pds[16];
+                tmem_ld32(tmem + lb + C::kTmS + 32 * c, sv);
+                tmem_ld32(tmem + lb + C::kTmP + 32 * c, dp);
+                p_ds_chunk(sv, dp, lse2 + 32 * c, dd + 32 * c, true, 0.f, 0.f, p.scale_log2,
+                           lim_lo, lim_hi, 32 * c, pp, pds);
+                tmem_st16(tmem + lb + C::kTmS + 16 * c, pp);
+                tmem_st16(tmem + lb + C::kTmP + 16 * c, pds);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v.p_full);
+        }
+        if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+        if (ok) {
+            tc_fence_after();
+            const bool in = key < N;
+            __nv_bfloat16 *dv = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
+            __nv_bfloat16 *dk = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], b[32], pa[16], pb[16];
+                tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
+                tmem_ld32(tmem + lb + C::kTmAcc1 + 32 * c, b);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
+                    pb[t] = pack_bf16x2(__uint_as_float(b[2 * t]) * p.scale,
+                                        __uint_as_float(b[2 * t + 1]) * p.scale);
+                }
+                if (in) {
+                    uint4 *o0 = reinterpret_cast<uint4 *>(dv + 32 * c);
+                    uint4 *o1 = reinterpret_cast<uint4 *>(dk + 32 * c);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        o0[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
+                        o1[t] = make_uint4(pb[4 * t], pb[4 * t + 1], pb[4 * t + 2], pb[4 * t + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ================================= dQ kernel =================================
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const Params p) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.n_blocks;
+    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
+                          : blockIdx.x % p.n_blocks;
+    const int N = p.N;
+    const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
+    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
+                                         v.abort_flag, C::kStages);
+    if (warp == kMmaWarp) {
+        tmem_alloc(v.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
+            mbar_arrive_expect_tx(v.once, 2 * C::kTile);
+            load_tile<D>(v.a, &tmQ, v.once, ib * kBlk, bh, pol_q);
+            load_tile<D>(v.b, &tmdO, v.once, ib * kBlk, bh, pol_q);
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < n_k && ok; ++t) {
+                const int s = t % C::kStages;
+                if (t >= C::kStages)
+                    ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
+                if (!ok) break;
+                uint8_t *st = v.ring + s * 2 * C::kTile;
+                mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
+                load_tile<D>(st, &tmK, &v.full[s], t * kBlk, bh, pol_kv);
+                load_tile<D>(st + C::kTile, &tmV, &v.full[s], t * kBlk, bh, pol_kv);
+                ++issued;
+            }
+            mbar_wait_drain(v.once, 0, p.limit_ns);
+            for (int t = max(0, issued - C::kStages); t < issued; ++t)
+                mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        const uint64_t dQ = sdesc_sw128(smem_u32(v.a), 16, 1024);
+        const uint64_t ddO = sdesc_sw128(smem_u32(v.b), 16, 1024);
+        const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
+        const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
+        const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+        };
+        bool ok = wait(v.once, 0, kSiteKV);
+        if (ok) tc_fence_after();
+        for (int t = 0; t < n_k && ok; ++t) {
+            const int s = t % C::kStages;
+            ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
+            const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+            mma_rows_rows<D>(tmem + C::kTmS, dQ, ring_k + so);         // S = Q K^T
+            mma_rows_rows<D>(tmem + C::kTmP, ddO, ring_k + so + to);   // dP = dO V^T
+            mma_commit_elect(v.s_full);
+            ok = wait(v.p_full, t & 1, kSiteP);
+            if (!ok) break;
+            tc_fence_after();
+            mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so, t > 0);  // dQ += dS K
+            mma_commit_elect(&v.empty[s]);
+        }
+        mma_commit_elect(v.o_full);
+        mbar_wait_drain(v.o_full, 0, p.limit_ns);
+    } else {
+        const int row = warp * 32 + lane;
+        const int q = ib * kBlk + row;
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const bool qin = q < N;
+        const float my_lse2 = qin ? p.LSE[static_cast<size_t>(bh) * N + q] * kLog2e : 0.f;
+        const float my_d = qin ? p.Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_k && ok; ++t) {
+            ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+            if (!ok) break;
+            tc_fence_after();
+            const int k0 = t * kBlk;
+            // key k kept iff k < N and, causal, k <= q
+            const int lim_hi = CAUSAL ? min(N - k0, q - k0 + 1) : N - k0;
+#pragma unroll 1
+            for (int c = 0; c < kBlk / 32; ++c) {
+                uint32_t sv[32], dp[32], pp[16], pds[16];
+                tmem_ld32(tmem + lb + C::kTmS + 32 * c, sv);
+                tmem_ld32(tmem + lb + C::kTmP + 32 * c, dp);
+                p_ds_chunk(sv, dp, nullptr, nullptr, false, my_lse2, my_d, p.scale_log2, 0,
+                           lim_hi, 32 * c, pp, pds);
+                tmem_st16(tmem + lb + C::kTmS + 16 * c, pds);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v.p_full);
+        }
+        if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16 *dq = p.g0 + (static_cast<size_t>(bh) * N + q) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], pa[16];
+                tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale,
+                                        __uint_as_float(a[2 * t + 1]) * p.scale);
+                if (qin) {
+                    uint4 *o = reinterpret_cast<uint4 *>(dq + 32 * c);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        o[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D = rowsum(dO * O), one warp per row, fp32.
+template <int D>
+__global__ void pre_kernel(const __nv_bfloat16 *__restrict__ O,
+                           const __nv_bfloat16 *__restrict__ dO, float *__restrict__ Dvec,
+                           long long rows) {
+    constexpr int E = D / 32;
+    const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16 *o = O + row * D + lane * E;
+    const __nv_bfloat16 *g = dO + row * D + lane * E;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) Dvec[row] = acc;
+}
+
+}  // namespace bwd
+
+template <int D, bool CAUSAL>
+static int launch_bwd_t(const BwdArgs &a) {
+    using C = bwd::Cfg<D>;
+    static int configured[64] = {0};
+    int dev = 0;
+    FA_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
+    auto k1 = bwd::dkdv_kernel<D, CAUSAL>;
+    auto k2 = bwd::dq_kernel<D, CAUSAL>;
+    if (!configured[dev]) {
+        FA_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes));
+        FA_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes));
+        configured[dev] = 1;
+    }
+    const long long rows = static_cast<long long>(a.BH) * a.N;
+    bwd::pre_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.O), static_cast<const __nv_bfloat16 *>(a.dO),
+        a.Dvec, rows);
+    FA_CUDA_TRY(cudaGetLastError());
+    bwd::Params p;
+    p.LSE = a.LSE;
+    p.Dvec = a.Dvec;
+    p.N = a.N;
+    p.BH = a.BH;
+    p.n_blocks = (a.N + bwd::kBlk - 1) / bwd::kBlk;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * bwd::kLog2e;
+    p.limit_ns = a.limit_ns;
+    const long long grid = static_cast<long long>(p.n_blocks) * a.BH;
+    if (grid > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
+    p.g0 = static_cast<__nv_bfloat16 *>(a.dK);
+    p.g1 = static_cast<__nv_bfloat16 *>(a.dV);
+    k1<<<static_cast<unsigned>(grid), bwd::kThreads, C::kSmemBytes, a.stream>>>(
+        *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, p);
+    FA_CUDA_TRY(cudaGetLastError());
+    p.g0 = static_cast<__nv_bfloat16 *>(a.dQ);
+    p.g1 = nullptr;
+    k2<<<static_cast<unsigned>(grid), bwd::kThreads, C::kSmemBytes, a.stream>>>(
+        *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, p);
+    FA_CUDA_TRY(cudaGetLastError());
+    return FA_OK;
+}
+
+int launch_bwd(const BwdArgs &a) {
+    if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);
+    if (a.d == 128) return a.causal ? launch_bwd_t<128, true>(a) : launch_bwd_t<128, false>(a);
+    return FA_ERR_HEADDIM;
+}
+
+int bwd_read_and_clear_status(int *status) {
+    int v = 0;
+    FA_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_fa_status_bwd, sizeof v));
+    if (v != 0) {
+        const int zero = 0;
+        FA_CUDA_TRY(cudaMemcpyToSymbol(g_fa_status_bwd, &zero, sizeof zero));
+    }
+    *status = v;
+    return FA_OK;
+}
+
+}  // namespace fa

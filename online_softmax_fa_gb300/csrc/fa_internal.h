@@ -25,6 +25,22 @@ struct LaunchArgs {
 
 int launch_fwd(const LaunchArgs &a);
 
+// Backward pass (fa_bwd_sm103.cu).
+struct BwdArgs {
+    const CUtensorMap *tmQ, *tmK, *tmV, *tmdO;
+    const void *O, *dO;          // bf16 [BH, N, d]
+    const float *LSE;            // fp32 [BH, N] (natural log)
+    float *Dvec;                 // fp32 [BH, N] scratch: rowsum(dO * O)
+    void *dQ, *dK, *dV;          // bf16 [BH, N, d]
+    int BH, N, d;
+    bool causal;
+    float scale;
+    uint64_t limit_ns;
+    cudaStream_t stream;
+};
+int launch_bwd(const BwdArgs &a);
+int bwd_read_and_clear_status(int *status);
+
 // Split-KV decoding (fa_decode_sm103.cu).
 struct DecodeArgs {
     const void *Q, *K, *V;  // bf16 [B,H,d], [B,H_kv,N,d], [B,H_kv,N,d]

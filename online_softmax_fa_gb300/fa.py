@@ -48,6 +48,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_host_workspace_bytes.restype = S
     lib.fa_fwd_host.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
     lib.fa_fwd_host.restype = I
+    lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    lib.fa_bwd_workspace_bytes.restype = S
+    lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, S, I, I, I, I, I, F, P]
+    lib.fa_bwd.restype = I
     lib.fa_decode_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.fa_decode_workspace_bytes.restype = S
     lib.fa_decode.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
@@ -161,6 +165,38 @@ def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, workspace,
         B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_host")
+
+
+def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, workspace=None,
+           causal: bool = False, scale: float | None = None, stream=None):
+    """Gradients (dq, dk, dv) of fa_fwd for the output gradient ``do``.
+    q, k, v, o, do: contiguous CUDA bf16 [B, H, N, d]; lse: fp32 [B, H, N]
+    from the same forward call.  Outputs are allocated when not given."""
+    import torch
+    B, H, N, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    rc = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), B, H, N, d,
+                               1 if causal else 0, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, d))
 
 
 def fa_decode_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:

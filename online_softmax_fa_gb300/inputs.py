@@ -117,6 +117,16 @@ def make_workload(w: Workload):
     return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.k_row_ramp, w.H_kv)
 
 
+def make_grad(B: int, H: int, N: int, d: int, seed: int):
+    """Output gradient dO [B, H, N, d] for the backward pass: N(0,1) in fp32
+    from ``seed + 1000``, rounded to bf16 (its own stream, so Q, K, V of the
+    same seed are unchanged)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 1000)
+    return torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(
+        torch.bfloat16).contiguous()
+
+
 def fixed_edge_rows(N: int, tile: int = 128) -> list:
     """Rows at tile edges and the ragged tail that are always checked."""
     cand = {0, 1, tile - 1, tile, N - 1}

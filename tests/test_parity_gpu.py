@@ -294,3 +294,76 @@ def test_decode_matches_forward_last_row(fa):
     torch.cuda.synchronize()
     assert (o_f[:, :, -1].float() - o_d.float()).abs().max().item() <= 2 * O_MAX
     assert (l_f[:, :, -1] - l_d).abs().max().item() <= 2 * LSE_MAX
+
+
+# ------------------------------------------------------------ backward pass
+from online_softmax_fa_gb300.inputs import make_grad  # noqa: E402
+
+# Bounds for the bf16 gradients, relative to the size of each reference
+# gradient (max |ref| for the max error, mean |ref| for the mean error):
+# outputs are rounded to bf16 (<= 2^-9 relative each), P and dS are rounded
+# to bf16 for the tensor cores (<= 2^-9 per term), and dQ, dK are sums of dS
+# terms that cancel (each row of dS sums to zero), which amplifies those
+# roundings relative to the result (measured up to ~7e-3 mean at N = 2).
+# Gradients below G_FLOOR in size (N = 1 gives exact zeros) use the floor.
+G_MAX_REL, G_MEAN_REL, G_FLOOR = 2e-2, 1e-2, 1e-3
+
+
+def _bwd_run(fa, q, k, v, do, causal, scale):
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.fa_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    return tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
+
+
+def _grad_check(got, ref, what):
+    errs = []
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.isfinite(g).all(), f"{what} {name} not finite"
+        e = np.abs(g - r)
+        scale_max = max(np.abs(r).max(), G_FLOOR)
+        scale_mean = max(np.abs(r).mean(), G_FLOOR)
+        errs.append((name, e.max() / scale_max, e.mean() / scale_mean))
+        assert e.max() <= G_MAX_REL * scale_max, f"{what} {name}: max {e.max():.3e} ref {scale_max:.3e}"
+        assert e.mean() <= G_MEAN_REL * scale_mean, f"{what} {name}: mean {e.mean():.3e} ref {scale_mean:.3e}"
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 300, 640])
+def test_backward_parity(fa, N, d, causal):
+    q, k, v = make_qkv(1, 2, N, d, seed=500 + N + d)
+    do = make_grad(1, 2, N, d, seed=500 + N + d)
+    got = _bwd_run(fa, q, k, v, do, causal, scale_of(d))
+    ref = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale_of(d))
+    errs = _grad_check(got, ref, f"bwd N={N} d={d} causal={causal}")
+    print(f"bwd N={N} d={d} causal={causal}: " + ", ".join(
+        f"{n} max {a:.2e} mean {b:.2e}" for n, a, b in errs))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_late_max_workload(fa, causal):
+    w = WORKLOADS["late"]
+    q, k, v = make_workload(w)
+    do = make_grad(w.B, w.H, w.N, w.d, w.seed)
+    got = _bwd_run(fa, q, k, v, do, causal, w.scale)
+    ref = oracle.attention_bwd(q, k, v, do, causal=causal, scale=w.scale)
+    errs = _grad_check(got, ref, f"bwd late causal={causal}")
+    print(f"bwd late causal={causal}: " + ", ".join(
+        f"{n} max {a:.2e} mean {b:.2e}" for n, a, b in errs))
+
+
+def test_backward_deterministic(fa):
+    q, k, v = make_qkv(2, 3, 700, 128, seed=77)
+    do = make_grad(2, 3, 700, 128, seed=77)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd(qd, kd, vd, causal=True)
+    a = fa.fa_bwd(qd, kd, vd, o, lse, dod, causal=True)
+    b = fa.fa_bwd(qd, kd, vd, o, lse, dod, causal=True)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
