@@ -161,9 +161,10 @@ size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int N, int d);
  * key/value cache: O = softmax(scale * q K^T) V and LSE, every cached key
  * visible.  Decoding has no query-block parallelism ("FlashAttention-2 --
  * Deeper Math", "What FA-2 does not fix"), so the keys are split across
- * warps, each keeps the online-softmax state of "Understanding
- * FlashAttention Pt 1", section 2.4, for its split, and a second kernel
- * merges the splits with the same rule.
+ * the GPU: every SM streams an equal run of the cache, its warps keep the
+ * online-softmax state of "Understanding FlashAttention Pt 1", section 2.4,
+ * for their keys, and a second kernel merges the partial states with the
+ * same rule.  The workspace size depends on B, H and H_kv only.
  *
  *   Q, O     bf16 [B, H, d] (the newest token of each sequence and head)
  *   K, V     bf16 [B, H_kv, N, d], N cached positions

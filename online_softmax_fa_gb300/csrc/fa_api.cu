@@ -72,6 +72,24 @@ bool encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K/V cache [B*H_kv, N, d] bf16 for decoding: box = all d columns x 64 rows
+// x 1 head, no swizzle (rows land contiguously in shared memory), rows past N
+// read as zero.
+bool encode_cache_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -200,15 +218,15 @@ int check_decode_shape(int B, int H, int H_kv, int N, int d, float scale) {
     if (H % H_kv != 0) return FA_ERR_SHAPE;
     const int G = H / H_kv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return FA_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * H_kv > 65535) return FA_ERR_SHAPE;  // grid.y
+    if (static_cast<long long>(B) * H_kv > 65535) return FA_ERR_SHAPE;  // bounds the tile arithmetic
     if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_SCALE;
     return FA_OK;
 }
 
 // workspace layout: partial accumulators, then partial (m, l) pairs
 void decode_layout(int B, int H, int H_kv, int N, int d, size_t *acc_bytes, size_t *ml_bytes) {
-    const size_t states = static_cast<size_t>(B) * H_kv * fa::decode_n_splits(B, H_kv, N) *
-                          (H / H_kv);
+    (void)N;  // the state count depends on the heads only
+    const size_t states = fa::decode_state_count(B, H, H_kv);
     *acc_bytes = align256(states * d * sizeof(float));
     *ml_bytes = align256(states * 2 * sizeof(float));
 }
@@ -251,10 +269,13 @@ int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
         return FA_ERR_ALIAS;
     rc = check_arch();
     if (rc != FA_OK) return rc;
+    CUtensorMap tmK, tmV;
+    if (!encode_cache_map(&tmK, K, B * H_kv, N, d) || !encode_cache_map(&tmV, V, B * H_kv, N, d))
+        return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed for K/V");
     fa::DecodeArgs a;
+    a.tmK = &tmK;
+    a.tmV = &tmV;
     a.Q = Q;
-    a.K = K;
-    a.V = V;
     a.O = O;
     a.LSE = LSE;
     a.part_acc = static_cast<float *>(workspace);
@@ -265,6 +286,7 @@ int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
     a.N = N;
     a.d = d;
     a.scale = scale;
+    a.limit_ns = kWaitLimitNs;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     return fa::launch_decode(a);
 }
@@ -353,12 +375,14 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
 }
 
 int fa_device_error(fa_stream_t stream) {
-    int v = 0, vb = 0;
+    int v = 0, vb = 0, vd = 0;
     int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
     if (rc != FA_OK) return rc;
     rc = fa::bwd_read_and_clear_status(&vb);
     if (rc != FA_OK) return rc;
-    return (v == 0 && vb == 0) ? FA_OK : FA_ERR_TIMEOUT;
+    rc = fa::dec_read_and_clear_status(&vd);
+    if (rc != FA_OK) return rc;
+    return (v == 0 && vb == 0 && vd == 0) ? FA_OK : FA_ERR_TIMEOUT;
 }
 
 int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {

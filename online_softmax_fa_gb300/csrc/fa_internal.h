@@ -43,17 +43,21 @@ int bwd_read_and_clear_status(int *status);
 
 // Split-KV decoding (fa_decode_sm103.cu).
 struct DecodeArgs {
-    const void *Q, *K, *V;  // bf16 [B,H,d], [B,H_kv,N,d], [B,H_kv,N,d]
+    const CUtensorMap *tmK, *tmV;  // K, V as [B*H_kv, N, d], 64-row boxes
+    const void *Q;          // bf16 [B,H,d]
     void *O;                // bf16 [B,H,d]
     float *LSE;             // fp32 [B,H]
-    float *part_acc;        // fp32 [B*H_kv, n_splits, G, d]
-    float *part_ml;         // fp32 [B*H_kv, n_splits, G, 2]
+    float *part_acc;        // fp32 [B*H_kv, slots, G, d]
+    float *part_ml;         // fp32 [B*H_kv, slots, G, 2]
     int B, H, H_kv, N, d;
     float scale;
+    uint64_t limit_ns;      // bound on every in-kernel wait
     cudaStream_t stream;
 };
 int launch_decode(const DecodeArgs &a);
-int decode_n_splits(int B, int H_kv, int N);
+// Partial softmax states a decoding workspace holds (device-independent).
+size_t decode_state_count(int B, int H, int H_kv);
+int dec_read_and_clear_status(int *status);
 // Device address and size of the library-owned scratch area that
 // fa_decode_noalloc uses (resolved once per device).
 int decode_static_scratch(void **ptr, size_t *bytes);
