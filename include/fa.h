@@ -119,8 +119,9 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host,
                 int causal, float scale, fa_stream_t stream);
 
 /*
- * fa_bwd_workspace_bytes -- device workspace fa_bwd needs: one fp32 per
- * query row (D_i = sum_r dO_ir O_ir), 256-byte aligned.  0 if invalid.
+ * fa_bwd_workspace_bytes -- device workspace fa_bwd needs: two fp32 per
+ * query row (D_i = sum_r dO_ir O_ir and LSE_i log2 e), rows padded to a
+ * multiple of 128 per head, 256-byte aligned.  0 if invalid.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 

@@ -315,7 +315,9 @@ int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, floa
 // ------------------------------------------------------------ backward
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
-    return align256(static_cast<size_t>(B) * H * N * sizeof(float));
+    // two fp32 values per query row, rows padded to a multiple of 128 per head
+    const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+    return align256(2 * static_cast<size_t>(B) * H * npad * sizeof(float));
 }
 
 int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
@@ -360,7 +362,7 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
     a.O = O;
     a.dO = dO;
     a.LSE = LSE;
-    a.Dvec = static_cast<float *>(workspace);
+    a.rows = static_cast<float *>(workspace);
     a.dQ = dQ;
     a.dK = dK;
     a.dV = dV;

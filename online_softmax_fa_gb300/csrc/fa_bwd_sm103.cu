@@ -10,20 +10,24 @@
 // with D_i = sum_r dO_ir O_ir.
 //
 // Three kernels, all deterministic (no atomics, fixed summation order):
-//   * pre:  D = rowsum(dO * O) in fp32, one warp per row.
+//   * pre:  D = rowsum(dO * O) in fp32 and LSE * log2(e), one warp per row,
+//           into rows padded to a multiple of 128 per head (the workspace)
+//           so that the dkdv producer fetches a block's rows with bulk copies.
 //   * dkdv: one CTA per (b, h, 128-key block j), query blocks i as the inner
 //           loop.  On tcgen05 with TMEM accumulators: S^T = K_j Q_i^T and
-//           dP^T = V_j dO_i^T (keys are the MMA rows), then four elementwise
-//           warps (thread = key row = TMEM lane) form P^T and dS^T in bf16
-//           over the S^T / dP^T columns, then dV_j += P^T dO_i and
+//           dP^T = V_j dO_i^T (keys are the MMA rows), then eight elementwise
+//           warps (thread = key row = TMEM lane, two warps per row, 64
+//           columns each) form P^T and dS^T in bf16 over the S^T / dP^T
+//           columns, then dV_j += P^T dO_i and
 //           dK_j += dS^T Q_i read them from TMEM.
 //   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
 //           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
 //           then dQ_i += dS K_j.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
 // is masked.  TMEM (dkdv): S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d, 256+2d); P^T and dS^T are bf16 over the first 64 columns of
-// S^T and dP^T.  TMEM (dq): S [0,128), dP [128,256), dQ [256,256+d).
+// dK [256+d, 256+2d); P^T and dS^T are bf16 pairs over columns [0,32) and
+// [64,96) of S^T and dP^T (each column-half warp writes over its own first
+// 32 columns).  TMEM (dq): S [0,128), dP [128,256), dQ [256,256+d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,9 +47,13 @@ namespace bwd {
 
 constexpr int kBlk = 128;             // rows per block (keys or queries)
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
-constexpr int kThreads = 192;         // 4 elementwise warps + MMA + TMA
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
+constexpr int kEwWarps = 8;           // elementwise warps: 4 lane quarters x 2 column halves
+constexpr int kThreads = 384;         // 3 warpgroups: 8 elementwise warps, MMA, TMA, 2 idle
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+// Registers after reallocation: 128 x (216 + 216 + 64) = 63488 <= 384 x 168.
+constexpr uint32_t kRegsEw = 216;
+constexpr uint32_t kRegsCtl = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -73,7 +81,10 @@ struct Cfg {
 
 struct Params {
     __nv_bfloat16 *g0, *g1;  // dkdv: dK, dV; dq: dQ
-    const float *LSE, *Dvec;
+    // per query row, padded to n_blocks * 128 rows per head (zeros past N),
+    // negated so that the elementwise step adds them:
+    const float *lse2;  // -LSE * log2(e)
+    const float *dd;    // -D, D = rowsum(dO * O)
     int N, BH, n_blocks;
     float scale, scale_log2;
     uint64_t limit_ns;
@@ -122,12 +133,16 @@ __device__ __forceinline__ void mma_rows_rows(uint32_t d_tm, uint64_t da, uint64
 }
 
 // acc[M128 x N(D)] (+)= A[tmem, 128 x 128 bf16] * B[128 rows x D, MN-major].
+// A's bf16 pairs sit in two column groups (written by the two column-half
+// warps over their own fp32 columns): K-steps 0-3 at columns [0, 32), 4-7
+// at [64, 96) of the region.
 template <int D>
 __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tm, uint32_t a_tm, uint64_t db, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < kBlk / 16; ++kk)
-        mma_ts_elect(d_tm, a_tm + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-                     Cfg<D>::kIdescAcc, (acc || kk > 0) ? 1u : 0u);
+        mma_ts_elect(d_tm, a_tm + (kk >> 2) * 64 + (kk & 3) * 8,
+                     db + static_cast<uint64_t>((kk * 16 * 128) >> 4), Cfg<D>::kIdescAcc,
+                     (acc || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -148,20 +163,59 @@ __device__ __forceinline__ void setup_barriers(uint64_t *once, uint64_t *full, u
         mbar_init(&empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 4);
+    mbar_init(p_full, kEwWarps);
     mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
 }
 
-// Elementwise part shared by both kernels: for 32 consecutive columns,
-// p = 2^(s*c - lse2) (0 where masked), ds = p * (dp - D); returns packed bf16
-// p and ds.  lse2/dd give the per-column (dkdv) or per-row (dq) statistics.
-__device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                           const float *lse2, const float *dd, bool col_stats,
-                                           float my_lse2, float my_d, float cs, int lim_lo,
-                                           int lim_hi, int col0, uint32_t (&pp)[16],
-                                           uint32_t (&pds)[16]) {
+// Elementwise part shared by both kernels, for 32 consecutive columns:
+// p = 2^(s*c - lse2), ds = p * (dp - D), returned as packed bf16 pairs.  The
+// statistics come negated (nl2 = -lse2, nd = -D): per column from shared
+// memory in dkdv (col_stats), per row in registers in dq.
+// Fast path (no column masked): packed fp32x2 arithmetic, 16-byte loads.
+__device__ __forceinline__ void p_ds_fast(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                          const float *nl2, const float *nd, bool col_stats,
+                                          float my_nl2, float my_nd, float cs,
+                                          uint32_t (&pp)[16], uint32_t (&pds)[16]) {
+    const uint64_t cs2 = f2_pack(cs, cs);
+#pragma unroll
+    for (int t4 = 0; t4 < 8; ++t4) {  // four columns at a time
+        float4 l4, d4;
+        if (col_stats) {
+            l4 = *reinterpret_cast<const float4 *>(nl2 + 4 * t4);
+            d4 = *reinterpret_cast<const float4 *>(nd + 4 * t4);
+        } else {
+            l4 = make_float4(my_nl2, my_nl2, my_nl2, my_nl2);
+            d4 = make_float4(my_nd, my_nd, my_nd, my_nd);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = 2 * t4 + h, e = 2 * t;
+            const uint64_t nl = h ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y);
+            const uint64_t nm = h ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), cs2, nl),
+                      x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const uint64_t p2 = f2_pack(p0, p1);
+            float ds0, ds1;
+            f2_unpack(f2_mul(p2, f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                        nm)),
+                      ds0, ds1);
+            pp[t] = pack_bf16x2(p0, p1);
+            pds[t] = pack_bf16x2(ds0, ds1);
+        }
+    }
+}
+
+// Masked path (diagonal or ragged block): column col0 + e is kept iff
+// lim_lo <= col0 + e < lim_hi; p = 0 elsewhere.
+__device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                            const float *nl2, const float *nd, bool col_stats,
+                                            float my_nl2, float my_nd, float cs, int lim_lo,
+                                            int lim_hi, int col0, uint32_t (&pp)[16],
+                                            uint32_t (&pds)[16]) {
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
         float p[2], ds[2];
@@ -169,11 +223,11 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32
         for (int u = 0; u < 2; ++u) {
             const int e = 2 * t + u;
             const int col = col0 + e;
-            const float l2 = col_stats ? lse2[e] : my_lse2;
-            const float dv = col_stats ? dd[e] : my_d;
+            const float l2 = col_stats ? nl2[e] : my_nl2;
+            const float dv = col_stats ? nd[e] : my_nd;
             const bool keep = col >= lim_lo && col < lim_hi;
-            p[u] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), cs, -l2)) : 0.f;
-            ds[u] = p[u] * (__uint_as_float(dp[e]) - dv);
+            p[u] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), cs, l2)) : 0.f;
+            ds[u] = p[u] * (__uint_as_float(dp[e]) + dv);
         }
         pp[t] = pack_bf16x2(p[0], p[1]);
         pds[t] = pack_bf16x2(ds[0], ds[1]);
@@ -182,6 +236,187 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32
 
 // ============================== dK / dV kernel ==============================
 template <int D, bool CAUSAL>
+__device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                                            const CUtensorMap *tmV, const CUtensorMap *tmdO,
+                                            const Params &p, int lane) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int jb = blockIdx.x % p.n_blocks;  // key block
+    const int N = p.N;
+    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
+    const int n_q = p.n_blocks - i0;
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    // ---- producer: K_j, V_j once; per query block Q_i, dO_i (TMA) and
+    // the block's LSE2 and D rows (bulk copies of the padded rows), all
+    // completing the stage's barrier
+    if (lane == 0) {
+        const uint64_t pol = l2_policy_evict_last();
+        mbar_arrive_expect_tx(v.once, 2 * C::kTile);
+        load_tile<D>(v.a, tmK, v.once, jb * kBlk, bh, pol);
+        load_tile<D>(v.b, tmV, v.once, jb * kBlk, bh, pol);
+        const size_t prow = static_cast<size_t>(bh) * p.n_blocks * kBlk;
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < n_q && ok; ++t) {
+            const int s = t % C::kStages;
+            if (t >= C::kStages)
+                ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
+            if (!ok) break;
+            const int q0 = (i0 + t) * kBlk;
+            float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
+            uint8_t *st = v.ring + s * 2 * C::kTile;
+            mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile + 2 * kBlk * 4);
+            load_tile<D>(st, tmQ, &v.full[s], q0, bh, pol);
+            load_tile<D>(st + C::kTile, tmdO, &v.full[s], q0, bh, pol);
+            bulk_load(lse2, p.lse2 + prow + q0, kBlk * 4, &v.full[s], pol);
+            bulk_load(dd, p.dd + prow + q0, kBlk * 4, &v.full[s], pol);
+            ++issued;
+        }
+        // drain the loads in flight
+        mbar_wait_drain(v.once, 0, p.limit_ns);
+        for (int t = max(0, issued - C::kStages); t < issued; ++t)
+            mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+    }
+    __syncwarp();
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dkdv_mma(const Params &p) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int jb = blockIdx.x % p.n_blocks;  // key block
+    const int N = p.N;
+    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
+    const int n_q = p.n_blocks - i0;
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    // ---- MMA issuer (converged warp, elected lane)
+    const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
+    const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
+    const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
+    const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+    };
+    bool ok = wait(v.once, 0, kSiteKV);
+    if (ok) tc_fence_after();
+    for (int t = 0; t < n_q && ok; ++t) {
+        const int s = t % C::kStages;
+        ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
+        const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+        mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so);        // S^T = K Q^T
+        mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so + to);   // dP^T = V dO^T
+        mma_commit_elect(v.s_full);
+        ok = wait(v.p_full, t & 1, kSiteP);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0);  // dV
+        mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmP, ring_mn + so, t > 0);       // dK
+        mma_commit_elect(&v.empty[s]);
+    }
+    mma_commit_elect(v.o_full);
+    mbar_wait_drain(v.o_full, 0, p.limit_ns);
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int lane) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int jb = blockIdx.x % p.n_blocks;  // key block
+    const int N = p.N;
+    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
+    const int n_q = p.n_blocks - i0;
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    // ---- elementwise: thread = key row of this block (TMEM lane), warp
+    // half h = columns (queries) [64h, 64h + 64)
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const int key = jb * kBlk + row;
+    const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    const int cb = half * 64;
+    bool ok = true;
+    for (int t = 0; t < n_q && ok; ++t) {
+        const int s = t % C::kStages;
+        ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+        // the stage's LSE2/D rows landed with its tiles (the stage cannot
+        // be refilled before this block's p_full)
+        if (ok) ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
+        if (!ok) break;
+        tc_fence_after();
+        const int q0 = (i0 + t) * kBlk;
+        const float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
+        // column (query) q kept iff q < N and, causal, q >= key
+        const int lim_lo = CAUSAL ? key - q0 : 0;
+        const int lim_hi = N - q0;
+        // this warp's 64 columns of S^T and dP^T in one round trip; P^T
+        // and dS^T (bf16 pairs) go over the first 32 of those columns
+        uint32_t s0[32], s1[32], d0[32], d1[32], pp[16], pds[16];
+        const uint32_t ts = tmem + lb + C::kTmS + cb, tp = tmem + lb + C::kTmP + cb;
+        tmem_ld32x4(ts, ts + 32, tp, tp + 32, s0, s1, d0, d1);
+        // masked only on the diagonal block (causal) and a ragged last block
+        const bool masked = (CAUSAL && t == 0) || q0 + kBlk > N;
+        if (masked)
+            p_ds_masked(s0, d0, lse2 + cb, dd + cb, true, 0.f, 0.f, p.scale_log2, lim_lo,
+                        lim_hi, cb, pp, pds);
+        else
+            p_ds_fast(s0, d0, lse2 + cb, dd + cb, true, 0.f, 0.f, p.scale_log2, pp, pds);
+        tmem_st16(ts, pp);
+        tmem_st16(tp, pds);
+        if (masked)
+            p_ds_masked(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2,
+                        lim_lo, lim_hi, cb + 32, pp, pds);
+        else
+            p_ds_fast(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2, pp,
+                      pds);
+        tmem_st16(ts + 16, pp);
+        tmem_st16(tp + 16, pds);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v.p_full);
+    }
+    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) {
+        tc_fence_after();
+        const bool in = key < N;
+        __nv_bfloat16 *dv = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
+        __nv_bfloat16 *dk = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
+#pragma unroll 1
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {  // half the columns
+            uint32_t a[32], b[32], pa[16], pb[16];
+            tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
+            tmem_ld32(tmem + lb + C::kTmAcc1 + 32 * c, b);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
+                pb[t] = pack_bf16x2(__uint_as_float(b[2 * t]) * p.scale,
+                                    __uint_as_float(b[2 * t + 1]) * p.scale);
+            }
+            if (in) {
+                uint4 *o0 = reinterpret_cast<uint4 *>(dv + 32 * c);
+                uint4 *o1 = reinterpret_cast<uint4 *>(dk + 32 * c);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    o0[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
+                    o1[t] = make_uint4(pb[4 * t], pb[4 * t + 1], pb[4 * t + 2], pb[4 * t + 3]);
+                }
+            }
+        }
+    }
+}
+
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -189,11 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     const View<D> v = view<D>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.n_blocks;
-    const int jb = blockIdx.x % p.n_blocks;  // key block
-    const int N = p.N;
-    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
-    const int n_q = p.n_blocks - i0;
     if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
                                          v.abort_flag, C::kStages);
     if (warp == kMmaWarp) {
@@ -203,151 +433,182 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *v.tmem_slot;
-    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
 
-    if (warp == kTmaWarp) {
-        // ---- producer: K_j, V_j once; per query block Q_i, dO_i (TMA) and
-        // LSE2_i, D_i (plain loads by the whole warp, bounds-checked)
-        const uint64_t pol = l2_policy_evict_last();
-        if (lane == 0) {
-            mbar_arrive_expect_tx(v.once, 2 * C::kTile);
-            load_tile<D>(v.a, &tmK, v.once, jb * kBlk, bh, pol);
-            load_tile<D>(v.b, &tmV, v.once, jb * kBlk, bh, pol);
-        }
-        int issued = 0;
-        bool ok = true;
-        for (int t = 0; t < n_q && ok; ++t) {
-            const int s = t % C::kStages;
-            if (t >= C::kStages)
-                ok = __all_sync(0xffffffffu, mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1,
-                                                       ctl, kSiteEmpty));
-            if (!ok) break;
-            const int q0 = (i0 + t) * kBlk;
-            float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
-            for (int e = lane; e < kBlk; e += 32) {
-                const int q = q0 + e;
-                const bool in = q < N;
-                lse2[e] = in ? p.LSE[static_cast<size_t>(bh) * N + q] * kLog2e : 0.f;
-                dd[e] = in ? p.Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                uint8_t *st = v.ring + s * 2 * C::kTile;
-                mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
-                load_tile<D>(st, &tmQ, &v.full[s], q0, bh, pol);
-                load_tile<D>(st + C::kTile, &tmdO, &v.full[s], q0, bh, pol);
-            }
-            ++issued;
-        }
-        if (lane == 0) {  // drain the loads in flight
-            mbar_wait_drain(v.once, 0, p.limit_ns);
-            for (int t = max(0, issued - C::kStages); t < issued; ++t)
-                mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
-        }
+    // Each role runs inside the branch that set its register budget and
+    // rebuilds what it needs, so little stays live across the switch.
+    if (warp >= kMmaWarp) {
+        regs_decrease<kRegsCtl>();  // warps 10, 11: no role
+        if (warp == kTmaWarp)
+            dkdv_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, &tmdO, p, lane);
+        else if (warp == kMmaWarp)
+            dkdv_mma<D, CAUSAL>(p);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ---- MMA issuer (converged warp, elected lane)
-        const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
-        const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
-        const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
-        const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
-        const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
-        };
-        bool ok = wait(v.once, 0, kSiteKV);
-        if (ok) tc_fence_after();
-        for (int t = 0; t < n_q && ok; ++t) {
-            const int s = t % C::kStages;
-            ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
-            const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
-            mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so);        // S^T = K Q^T
-            mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so + to);   // dP^T = V dO^T
-            mma_commit_elect(v.s_full);
-            ok = wait(v.p_full, t & 1, kSiteP);
-            if (!ok) break;
-            tc_fence_after();
-            mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0);  // dV
-            mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmP, ring_mn + so, t > 0);       // dK
-            mma_commit_elect(&v.empty[s]);
-        }
-        mma_commit_elect(v.o_full);
-        mbar_wait_drain(v.o_full, 0, p.limit_ns);
     } else {
-        // ---- elementwise: thread = key row r of this block
-        const int row = warp * 32 + lane;
-        const int key = jb * kBlk + row;
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-        bool ok = true;
-        for (int t = 0; t < n_q && ok; ++t) {
-            const int s = t % C::kStages;
-            ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
-            // the producer's LSE/D rows of this stage: observe them directly
-            // (the stage cannot be refilled before this block's p_full)
-            if (ok) ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
-            if (!ok) break;
-            tc_fence_after();
-            const int q0 = (i0 + t) * kBlk;
-            const float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
-            // column (query) q kept iff q < N and, causal, q >= key
-            const int lim_lo = CAUSAL ? key - q0 : 0;
-            const int lim_hi = N - q0;
-#pragma unroll 1
-            for (int c = 0; c < kBlk / 32; ++c) {
-                uint32_t sv[32], dp[32], pp[16], pds[16];
-                tmem_ld32(tmem + lb + C::kTmS + 32 * c, sv);
-                tmem_ld32(tmem + lb + C::kTmP + 32 * c, dp);
-                p_ds_chunk(sv, dp, lse2 + 32 * c, dd + 32 * c, true, 0.f, 0.f, p.scale_log2,
-                           lim_lo, lim_hi, 32 * c, pp, pds);
-                tmem_st16(tmem + lb + C::kTmS + 16 * c, pp);
-                tmem_st16(tmem + lb + C::kTmP + 16 * c, pds);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(v.p_full);
-        }
-        if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
-        if (ok) {
-            tc_fence_after();
-            const bool in = key < N;
-            __nv_bfloat16 *dv = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
-            __nv_bfloat16 *dk = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], b[32], pa[16], pb[16];
-                tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
-                tmem_ld32(tmem + lb + C::kTmAcc1 + 32 * c, b);
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
-                    pb[t] = pack_bf16x2(__uint_as_float(b[2 * t]) * p.scale,
-                                        __uint_as_float(b[2 * t + 1]) * p.scale);
-                }
-                if (in) {
-                    uint4 *o0 = reinterpret_cast<uint4 *>(dv + 32 * c);
-                    uint4 *o1 = reinterpret_cast<uint4 *>(dk + 32 * c);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        o0[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
-                        o1[t] = make_uint4(pb[4 * t], pb[4 * t + 1], pb[4 * t + 2], pb[4 * t + 3]);
-                    }
-                }
-            }
-        }
+        regs_increase<kRegsEw>();
+        dkdv_elementwise<D, CAUSAL>(p, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(*view<D>().tmem_slot, kTmemCols);
     }
 }
 
 // ================================= dQ kernel =================================
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtensorMap *tmK,
+                                            const CUtensorMap *tmV, const CUtensorMap *tmdO,
+                                            const Params &p, int lane) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
+                          : blockIdx.x % p.n_blocks;
+    const int N = p.N;
+    const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    if (lane == 0) {
+        const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
+        mbar_arrive_expect_tx(v.once, 2 * C::kTile);
+        load_tile<D>(v.a, tmQ, v.once, ib * kBlk, bh, pol_q);
+        load_tile<D>(v.b, tmdO, v.once, ib * kBlk, bh, pol_q);
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < n_k && ok; ++t) {
+            const int s = t % C::kStages;
+            if (t >= C::kStages)
+                ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
+            if (!ok) break;
+            uint8_t *st = v.ring + s * 2 * C::kTile;
+            mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
+            load_tile<D>(st, tmK, &v.full[s], t * kBlk, bh, pol_kv);
+            load_tile<D>(st + C::kTile, tmV, &v.full[s], t * kBlk, bh, pol_kv);
+            ++issued;
+        }
+        mbar_wait_drain(v.once, 0, p.limit_ns);
+        for (int t = max(0, issued - C::kStages); t < issued; ++t)
+            mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+    }
+    __syncwarp();
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dq_mma(const Params &p) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
+                          : blockIdx.x % p.n_blocks;
+    const int N = p.N;
+    const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    const uint64_t dQ = sdesc_sw128(smem_u32(v.a), 16, 1024);
+    const uint64_t ddO = sdesc_sw128(smem_u32(v.b), 16, 1024);
+    const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
+    const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
+    const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+    };
+    bool ok = wait(v.once, 0, kSiteKV);
+    if (ok) tc_fence_after();
+    for (int t = 0; t < n_k && ok; ++t) {
+        const int s = t % C::kStages;
+        ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
+        const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+        mma_rows_rows<D>(tmem + C::kTmS, dQ, ring_k + so);         // S = Q K^T
+        mma_rows_rows<D>(tmem + C::kTmP, ddO, ring_k + so + to);   // dP = dO V^T
+        mma_commit_elect(v.s_full);
+        ok = wait(v.p_full, t & 1, kSiteP);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so, t > 0);  // dQ += dS K
+        mma_commit_elect(&v.empty[s]);
+    }
+    mma_commit_elect(v.o_full);
+    mbar_wait_drain(v.o_full, 0, p.limit_ns);
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int lane) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    const int bh = blockIdx.x / p.n_blocks;
+    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
+                          : blockIdx.x % p.n_blocks;
+    const int N = p.N;
+    const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)N, (void)tmem, (void)bh;
+    const int quarter = warp & 3, half = warp >> 2;  // half h: keys [64h, 64h + 64)
+    const int row = quarter * 32 + lane;
+    const int q = ib * kBlk + row;
+    const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    const int cb = half * 64;
+    const bool qin = q < N;
+    const size_t prow = static_cast<size_t>(bh) * p.n_blocks * kBlk + q;  // padded row
+    const float my_nl2 = p.lse2[prow];  // -LSE log2 e (zero past N)
+    const float my_nd = p.dd[prow];     // -D
+    bool ok = true;
+    for (int t = 0; t < n_k && ok; ++t) {
+        ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+        if (!ok) break;
+        tc_fence_after();
+        const int k0 = t * kBlk;
+        // key k kept iff k < N and, causal, k <= q
+        const int lim_hi = CAUSAL ? min(N - k0, q - k0 + 1) : N - k0;
+        uint32_t s0[32], s1[32], d0[32], d1[32], pp[16], pds[16];
+        const uint32_t ts = tmem + lb + C::kTmS + cb, tp = tmem + lb + C::kTmP + cb;
+        tmem_ld32x4(ts, ts + 32, tp, tp + 32, s0, s1, d0, d1);
+        // masked only on the diagonal block (causal) and a ragged last block
+        const bool masked = (CAUSAL && t == ib) || k0 + kBlk > N;
+        if (masked)
+            p_ds_masked(s0, d0, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, 0,
+                        lim_hi, cb, pp, pds);
+        else
+            p_ds_fast(s0, d0, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, pp, pds);
+        tmem_st16(ts, pds);
+        if (masked)
+            p_ds_masked(s1, d1, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, 0,
+                        lim_hi, cb + 32, pp, pds);
+        else
+            p_ds_fast(s1, d1, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, pp, pds);
+        tmem_st16(ts + 16, pds);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v.p_full);
+    }
+    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) {
+        tc_fence_after();
+        __nv_bfloat16 *dq = p.g0 + (static_cast<size_t>(bh) * N + q) * D;
+#pragma unroll 1
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {  // half the columns
+            uint32_t a[32], pa[16];
+            tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale,
+                                    __uint_as_float(a[2 * t + 1]) * p.scale);
+            if (qin) {
+                uint4 *o = reinterpret_cast<uint4 *>(dq + 32 * c);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    o[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
+            }
+        }
+    }
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -356,11 +617,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     const View<D> v = view<D>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.n_blocks;
-    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
-                          : blockIdx.x % p.n_blocks;
-    const int N = p.N;
-    const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
     if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
                                          v.abort_flag, C::kStages);
     if (warp == kMmaWarp) {
@@ -370,136 +626,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *v.tmem_slot;
-    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
 
-    if (warp == kTmaWarp) {
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(v.once, 2 * C::kTile);
-            load_tile<D>(v.a, &tmQ, v.once, ib * kBlk, bh, pol_q);
-            load_tile<D>(v.b, &tmdO, v.once, ib * kBlk, bh, pol_q);
-            int issued = 0;
-            bool ok = true;
-            for (int t = 0; t < n_k && ok; ++t) {
-                const int s = t % C::kStages;
-                if (t >= C::kStages)
-                    ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
-                if (!ok) break;
-                uint8_t *st = v.ring + s * 2 * C::kTile;
-                mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
-                load_tile<D>(st, &tmK, &v.full[s], t * kBlk, bh, pol_kv);
-                load_tile<D>(st + C::kTile, &tmV, &v.full[s], t * kBlk, bh, pol_kv);
-                ++issued;
-            }
-            mbar_wait_drain(v.once, 0, p.limit_ns);
-            for (int t = max(0, issued - C::kStages); t < issued; ++t)
-                mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
-        }
+    // Each role runs inside the branch that set its register budget and
+    // rebuilds what it needs, so little stays live across the switch.
+    if (warp >= kMmaWarp) {
+        regs_decrease<kRegsCtl>();  // warps 10, 11: no role
+        if (warp == kTmaWarp)
+            dq_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, &tmdO, p, lane);
+        else if (warp == kMmaWarp)
+            dq_mma<D, CAUSAL>(p);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        const uint64_t dQ = sdesc_sw128(smem_u32(v.a), 16, 1024);
-        const uint64_t ddO = sdesc_sw128(smem_u32(v.b), 16, 1024);
-        const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
-        const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
-        const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
-        };
-        bool ok = wait(v.once, 0, kSiteKV);
-        if (ok) tc_fence_after();
-        for (int t = 0; t < n_k && ok; ++t) {
-            const int s = t % C::kStages;
-            ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
-            const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
-            mma_rows_rows<D>(tmem + C::kTmS, dQ, ring_k + so);         // S = Q K^T
-            mma_rows_rows<D>(tmem + C::kTmP, ddO, ring_k + so + to);   // dP = dO V^T
-            mma_commit_elect(v.s_full);
-            ok = wait(v.p_full, t & 1, kSiteP);
-            if (!ok) break;
-            tc_fence_after();
-            mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so, t > 0);  // dQ += dS K
-            mma_commit_elect(&v.empty[s]);
-        }
-        mma_commit_elect(v.o_full);
-        mbar_wait_drain(v.o_full, 0, p.limit_ns);
     } else {
-        const int row = warp * 32 + lane;
-        const int q = ib * kBlk + row;
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-        const bool qin = q < N;
-        const float my_lse2 = qin ? p.LSE[static_cast<size_t>(bh) * N + q] * kLog2e : 0.f;
-        const float my_d = qin ? p.Dvec[static_cast<size_t>(bh) * N + q] : 0.f;
-        bool ok = true;
-        for (int t = 0; t < n_k && ok; ++t) {
-            ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
-            if (!ok) break;
-            tc_fence_after();
-            const int k0 = t * kBlk;
-            // key k kept iff k < N and, causal, k <= q
-            const int lim_hi = CAUSAL ? min(N - k0, q - k0 + 1) : N - k0;
-#pragma unroll 1
-            for (int c = 0; c < kBlk / 32; ++c) {
-                uint32_t sv[32], dp[32], pp[16], pds[16];
-                tmem_ld32(tmem + lb + C::kTmS + 32 * c, sv);
-                tmem_ld32(tmem + lb + C::kTmP + 32 * c, dp);
-                p_ds_chunk(sv, dp, nullptr, nullptr, false, my_lse2, my_d, p.scale_log2, 0,
-                           lim_hi, 32 * c, pp, pds);
-                tmem_st16(tmem + lb + C::kTmS + 16 * c, pds);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(v.p_full);
-        }
-        if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16 *dq = p.g0 + (static_cast<size_t>(bh) * N + q) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], pa[16];
-                tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale,
-                                        __uint_as_float(a[2 * t + 1]) * p.scale);
-                if (qin) {
-                    uint4 *o = reinterpret_cast<uint4 *>(dq + 32 * c);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        o[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
-                }
-            }
-        }
+        regs_increase<kRegsEw>();
+        dq_elementwise<D, CAUSAL>(p, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(*view<D>().tmem_slot, kTmemCols);
     }
 }
 
-// D = rowsum(dO * O), one warp per row, fp32.
+// Per query row, into rows padded to Npad (a multiple of 128) per head, so
+// that the other kernels fetch a block's rows with aligned bulk copies:
+// -D = -rowsum(dO * O) (fp32) and -LSE * log2(e); zeros for rows past N.
+// One warp per padded row.
 template <int D>
 __global__ void pre_kernel(const __nv_bfloat16 *__restrict__ O,
-                           const __nv_bfloat16 *__restrict__ dO, float *__restrict__ Dvec,
-                           long long rows) {
+                           const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ LSE,
+                           float *__restrict__ lse2, float *__restrict__ dd, int N, int Npad,
+                           long long rows_pad) {
     constexpr int E = D / 32;
-    const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const __nv_bfloat16 *o = O + row * D + lane * E;
-    const __nv_bfloat16 *g = dO + row * D + lane * E;
-    float acc = 0.f;
+    for (long long prow = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+         prow < rows_pad; prow += static_cast<long long>(gridDim.x) * 4) {
+        const long long bh = prow / Npad;
+        const int q = static_cast<int>(prow - bh * Npad);
+        float acc = 0.f, l2 = 0.f;
+        if (q < N) {
+            const long long row = bh * N + q;
+            const __nv_bfloat16 *o = O + row * D + lane * E;
+            const __nv_bfloat16 *g = dO + row * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+            for (int e = 0; e < E; ++e)
+                acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) Dvec[row] = acc;
+            for (int off = 16; off > 0; off >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            l2 = LSE[row] * kLog2e;
+        }
+        if (lane == 0) {
+            dd[prow] = -acc;
+            lse2[prow] = -l2;
+        }
+    }
 }
 
 }  // namespace bwd
@@ -520,17 +701,22 @@ static int launch_bwd_t(const BwdArgs &a) {
                                          C::kSmemBytes));
         configured[dev] = 1;
     }
-    const long long rows = static_cast<long long>(a.BH) * a.N;
-    bwd::pre_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, a.stream>>>(
+    const int n_blocks = (a.N + bwd::kBlk - 1) / bwd::kBlk;
+    const int Npad = n_blocks * bwd::kBlk;
+    const long long rows_pad = static_cast<long long>(a.BH) * Npad;
+    float *lse2 = a.rows, *dd = a.rows + rows_pad;
+    const long long pre_blocks = (rows_pad + 3) / 4;
+    bwd::pre_kernel<D><<<static_cast<unsigned>(pre_blocks < (1 << 20) ? pre_blocks : (1 << 20)),
+                         128, 0, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.O), static_cast<const __nv_bfloat16 *>(a.dO),
-        a.Dvec, rows);
+        a.LSE, lse2, dd, a.N, Npad, rows_pad);
     FA_CUDA_TRY(cudaGetLastError());
     bwd::Params p;
-    p.LSE = a.LSE;
-    p.Dvec = a.Dvec;
+    p.lse2 = lse2;
+    p.dd = dd;
     p.N = a.N;
     p.BH = a.BH;
-    p.n_blocks = (a.N + bwd::kBlk - 1) / bwd::kBlk;
+    p.n_blocks = n_blocks;
     p.scale = a.scale;
     p.scale_log2 = a.scale * bwd::kLog2e;
     p.limit_ns = a.limit_ns;

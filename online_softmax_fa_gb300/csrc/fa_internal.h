@@ -30,7 +30,7 @@ struct BwdArgs {
     const CUtensorMap *tmQ, *tmK, *tmV, *tmdO;
     const void *O, *dO;          // bf16 [BH, N, d]
     const float *LSE;            // fp32 [BH, N] (natural log)
-    float *Dvec;                 // fp32 [BH, N] scratch: rowsum(dO * O)
+    float *rows;                 // fp32 scratch [2][BH][Npad]: LSE*log2(e), rowsum(dO*O)
     void *dQ, *dK, *dV;          // bf16 [BH, N, d]
     int BH, N, d;
     bool causal;

@@ -114,6 +114,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// Contiguous global -> shared copy on the TMA engine: both addresses 16-byte
+// aligned, `bytes` a multiple of 16; completes `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -244,6 +255,8 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // .xN covers N consecutive 32-bit columns.  The load variants wait for
 // completion inside the same asm statement, so the outputs are valid when
 // the statement ends.
+#define FA_R8X(a, i) "=r"(a[i]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), \
+                     "=r"(a[i + 4]), "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 #define FA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
@@ -284,6 +297,32 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
         : "memory");
 }
 
+// Four x32 loads (any four 32-column groups of this warp's lanes), one wait.
+__device__ __forceinline__ void tmem_ld32x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t (&r)[32], uint32_t (&q)[32],
+                                            uint32_t (&u)[32], uint32_t (&w)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127},"
+        " [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : FA_R8X(r, 0), FA_R8X(r, 8), FA_R8X(r, 16), FA_R8X(r, 24), FA_R8X(q, 0), FA_R8X(q, 8),
+          FA_R8X(q, 16), FA_R8X(q, 24), FA_R8X(u, 0), FA_R8X(u, 8), FA_R8X(u, 16),
+          FA_R8X(u, 24), FA_R8X(w, 0), FA_R8X(w, 8), FA_R8X(w, 16), FA_R8X(w, 24)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -306,6 +345,7 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 #undef FA_R8
+#undef FA_R8X
 #undef FA_W8
 
 // ------------------------------------------------------- register budget
