@@ -22,12 +22,14 @@
 //           dK_j += dS^T Q_i read them from TMEM.
 //   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
 //           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
-//           then dQ_i += dS K_j.
+//           then dQ_i += dS K_j; S is double-buffered, so the next block's S
+//           and dP run on the tensor pipe while the warps work on this one.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
 // is masked.  TMEM (dkdv): S^T [0,128), dP^T [128,256), dV [256,256+d),
 // dK [256+d, 256+2d); P^T and dS^T are bf16 pairs over columns [0,32) and
 // [64,96) of S^T and dP^T (each column-half warp writes over its own first
-// 32 columns).  TMEM (dq): S [0,128), dP [128,256), dQ [256,256+d).
+// 32 columns).  TMEM (dq): S [0,128) and [128,256), dP [256,384),
+// dQ [384,384+d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -63,14 +65,24 @@ template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = kChunks * kBoxBytes;  // one [128 x D] bf16 tile
+    // dkdv: K_j, V_j once; a ring of kStages stages of (Q_i, dO_i) tiles and
+    // their LSE2 / D rows.  dq: Q_i, dO_i once; a ring of kStagesK K tiles and
+    // one of kStagesV V tiles (V is released as soon as dP has read it, K only
+    // after dQ, so K runs a stage further ahead).
     static constexpr int kStages = 2;
-    // dkdv: K_j, V_j once; Q_i, dO_i per stage; LSE2 and D per stage (floats)
+    static constexpr int kStagesK = 3, kStagesV = 2;
     static constexpr int kOffA = 0;                 // K_j (dkdv) / Q_i (dq)
     static constexpr int kOffB = kTile;             // V_j (dkdv) / dO_i (dq)
-    static constexpr int kOffRing = 2 * kTile;      // stages of two tiles each
-    static constexpr int kOffRows = kOffRing + kStages * 2 * kTile;  // LSE2, D per stage
-    static constexpr int kOffBar = kOffRows + kStages * 2 * kBlk * 4;
-    static constexpr int kNumBars = 1 + 2 * kStages + 3;  // once, full/empty[S], s, p, o
+    static constexpr int kOffRing = 2 * kTile;
+    static constexpr int kOffRows = kOffRing + kStages * 2 * kTile;  // dkdv: LSE2, D per stage
+    static constexpr int kRingDkdv = kStages * 2 * kTile + kStages * 2 * kBlk * 4;
+    static constexpr int kRingDq = (kStagesK + kStagesV) * kTile;
+    static constexpr int kOffVq = kOffRing + kStagesK * kTile;      // dq: V ring
+    static constexpr int kOffBar = kOffRing + (kRingDkdv > kRingDq ? kRingDkdv : kRingDq);
+    // once, full/empty[3] (dkdv: stages; dq: K ring), vfull/vempty[2] (dq: V
+    // ring), s_full[2], p_full, o_full, dp_free
+    static constexpr int kNumBars = 1 + 2 * 3 + 2 * 2 + 5;
+    static_assert(kStages <= 3 && kStagesK <= 3 && kStagesV <= 2, "barrier slots");
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static constexpr uint32_t kTmS = 0, kTmP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
@@ -78,6 +90,10 @@ struct Cfg {
     static constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBlk, D, true);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+
+// TMEM of the dQ kernel: S double-buffered, dP, dQ.
+constexpr uint32_t kTmSq = 0, kTmPq = 256, kTmAccq = 384;
+static_assert(kTmAccq + 128 <= kTmemCols, "TMEM budget of the dQ kernel");
 
 struct Params {
     __nv_bfloat16 *g0, *g1;  // dkdv: dK, dV; dq: dQ
@@ -94,7 +110,8 @@ template <int D>
 struct View {
     uint8_t *a, *b, *ring;
     float *rows;
-    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;
+    uint8_t *vring;  // dq: V ring
+    uint64_t *once, *full, *empty, *vfull, *vempty, *s_full, *p_full, *o_full, *dp_free;
     uint32_t *tmem_slot;
     volatile int *abort_flag;
 };
@@ -109,14 +126,18 @@ __device__ __forceinline__ View<D> view() {
     v.a = smem + C::kOffA;
     v.b = smem + C::kOffB;
     v.ring = smem + C::kOffRing;
+    v.vring = smem + C::kOffVq;
     v.rows = reinterpret_cast<float *>(smem + C::kOffRows);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
     v.once = bar;
     v.full = bar + 1;
-    v.empty = v.full + C::kStages;
-    v.s_full = v.empty + C::kStages;
-    v.p_full = v.s_full + 1;
+    v.empty = v.full + 3;
+    v.vfull = v.empty + 3;
+    v.vempty = v.vfull + 2;
+    v.s_full = v.vempty + 2;
+    v.p_full = v.s_full + 2;
     v.o_full = v.p_full + 1;
+    v.dp_free = v.o_full + 1;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     return v;
@@ -154,17 +175,24 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, ui
 }
 
 __device__ __forceinline__ void setup_barriers(uint64_t *once, uint64_t *full, uint64_t *empty,
+                                               uint64_t *vfull, uint64_t *vempty,
                                                uint64_t *s_full, uint64_t *p_full,
-                                               uint64_t *o_full, volatile int *abort_flag,
-                                               int stages) {
+                                               uint64_t *o_full, uint64_t *dp_free,
+                                               volatile int *abort_flag) {
     mbar_init(once, 1);
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < 3; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
     }
-    mbar_init(s_full, 1);
+    for (int s = 0; s < 2; ++s) {
+        mbar_init(&vfull[s], 1);
+        mbar_init(&vempty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_full, kEwWarps);
     mbar_init(o_full, 1);
+    mbar_init(dp_free, kEwWarps);
     *abort_flag = 0;
     fence_mbarrier_init();
 }
@@ -424,8 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     const View<D> v = view<D>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
-                                         v.abort_flag, C::kStages);
+    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.vfull, v.vempty, v.s_full, v.p_full,
+                                         v.o_full, v.dp_free,
+                                         v.abort_flag);
     if (warp == kMmaWarp) {
         tmem_alloc(v.tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -475,22 +504,28 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
         mbar_arrive_expect_tx(v.once, 2 * C::kTile);
         load_tile<D>(v.a, tmQ, v.once, ib * kBlk, bh, pol_q);
         load_tile<D>(v.b, tmdO, v.once, ib * kBlk, bh, pol_q);
-        int issued = 0;
+        int nk = 0, nv = 0;  // K and V tiles issued
         bool ok = true;
         for (int t = 0; t < n_k && ok; ++t) {
-            const int s = t % C::kStages;
-            if (t >= C::kStages)
-                ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
+            const int sk = t % C::kStagesK, sv = t % C::kStagesV;
+            if (t >= C::kStagesK)
+                ok = mbar_wait(&v.empty[sk], ((t / C::kStagesK) & 1) ^ 1, ctl, kSiteEmpty);
             if (!ok) break;
-            uint8_t *st = v.ring + s * 2 * C::kTile;
-            mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile);
-            load_tile<D>(st, tmK, &v.full[s], t * kBlk, bh, pol_kv);
-            load_tile<D>(st + C::kTile, tmV, &v.full[s], t * kBlk, bh, pol_kv);
-            ++issued;
+            mbar_arrive_expect_tx(&v.full[sk], C::kTile);
+            load_tile<D>(v.ring + sk * C::kTile, tmK, &v.full[sk], t * kBlk, bh, pol_kv);
+            ++nk;
+            if (t >= C::kStagesV)
+                ok = mbar_wait(&v.vempty[sv], ((t / C::kStagesV) & 1) ^ 1, ctl, kSiteEmpty);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&v.vfull[sv], C::kTile);
+            load_tile<D>(v.vring + sv * C::kTile, tmV, &v.vfull[sv], t * kBlk, bh, pol_kv);
+            ++nv;
         }
         mbar_wait_drain(v.once, 0, p.limit_ns);
-        for (int t = max(0, issued - C::kStages); t < issued; ++t)
-            mbar_wait_drain(&v.full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
+        for (int t = max(0, nk - C::kStagesK); t < nk; ++t)
+            mbar_wait_drain(&v.full[t % C::kStagesK], (t / C::kStagesK) & 1, p.limit_ns);
+        for (int t = max(0, nv - C::kStagesV); t < nv; ++t)
+            mbar_wait_drain(&v.vfull[t % C::kStagesV], (t / C::kStagesV) & 1, p.limit_ns);
     }
     __syncwarp();
 }
@@ -509,28 +544,56 @@ __device__ __forceinline__ void dq_mma(const Params &p) {
     (void)N, (void)tmem, (void)bh;
     const uint64_t dQ = sdesc_sw128(smem_u32(v.a), 16, 1024);
     const uint64_t ddO = sdesc_sw128(smem_u32(v.b), 16, 1024);
-    const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
-    const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
+    const uint64_t kring = sdesc_sw128(smem_u32(v.ring), 16, 1024);          // K, K-major
+    const uint64_t kring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);  // K, MN-major
+    const uint64_t vring = sdesc_sw128(smem_u32(v.vring), 16, 1024);         // V, K-major
+    const auto kofs = [](int t) {
+        return static_cast<uint64_t>(((t % C::kStagesK) * C::kTile) >> 4);
+    };
+    const auto vofs = [](int t) {
+        return static_cast<uint64_t>(((t % C::kStagesV) * C::kTile) >> 4);
+    };
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
+    // S(t) goes to buffer t % 2, so S(t+1) and dP(t+1) run on the tensor
+    // pipe while the elementwise warps work on block t: S(t+1) as soon as
+    // K(t+1) is in (its buffer held dS(t-1), read by dQ(t-1) issued before),
+    // dP(t+1) once the warps have read dP(t) (dp_free).
     bool ok = wait(v.once, 0, kSiteKV);
-    if (ok) tc_fence_after();
+    if (ok) ok = wait(&v.full[0], 0, kSiteQ);
+    if (ok) ok = wait(&v.vfull[0], 0, kSiteQ);
+    if (ok) {
+        tc_fence_after();
+        mma_rows_rows<D>(tmem + kTmSq, dQ, kring);   // S(0) = Q K_0^T
+        mma_rows_rows<D>(tmem + kTmPq, ddO, vring);  // dP(0) = dO V_0^T
+        mma_commit_elect(&v.vempty[0]);              // V_0 read
+        mma_commit_elect(&v.s_full[0]);
+    }
     for (int t = 0; t < n_k && ok; ++t) {
-        const int s = t % C::kStages;
-        ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
+        const int t1 = t + 1;
+        const bool more = t1 < n_k;
+        if (more) {
+            ok = wait(&v.full[t1 % C::kStagesK], (t1 / C::kStagesK) & 1, kSiteQ);
+            if (!ok) break;
+            tc_fence_after();
+            mma_rows_rows<D>(tmem + kTmSq + (t1 & 1) * kBlk, dQ, kring + kofs(t1));  // S(t+1)
+        }
+        ok = wait(v.dp_free, t & 1, kSiteP);
+        if (ok && more) ok = wait(&v.vfull[t1 % C::kStagesV], (t1 / C::kStagesV) & 1, kSiteQ);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
-        const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
-        mma_rows_rows<D>(tmem + C::kTmS, dQ, ring_k + so);         // S = Q K^T
-        mma_rows_rows<D>(tmem + C::kTmP, ddO, ring_k + so + to);   // dP = dO V^T
-        mma_commit_elect(v.s_full);
+        if (more) {
+            mma_rows_rows<D>(tmem + kTmPq, ddO, vring + vofs(t1));  // dP(t+1)
+            mma_commit_elect(&v.vempty[t1 % C::kStagesV]);          // V(t+1) read
+            mma_commit_elect(&v.s_full[t1 & 1]);
+        }
         ok = wait(v.p_full, t & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
-        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so, t > 0);  // dQ += dS K
-        mma_commit_elect(&v.empty[s]);
+        mma_tmem_rows<D>(tmem + kTmAccq, tmem + kTmSq + (t & 1) * kBlk, kring_mn + kofs(t),
+                         t > 0);  // dQ += dS(t) K(t)
+        mma_commit_elect(&v.empty[t % C::kStagesK]);  // K(t) read by S(t) and dQ(t)
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
@@ -559,15 +622,19 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
     const float my_nd = p.dd[prow];     // -D
     bool ok = true;
     for (int t = 0; t < n_k && ok; ++t) {
-        ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+        ok = mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
         const int k0 = t * kBlk;
         // key k kept iff k < N and, causal, k <= q
         const int lim_hi = CAUSAL ? min(N - k0, q - k0 + 1) : N - k0;
         uint32_t s0[32], s1[32], d0[32], d1[32], pp[16], pds[16];
-        const uint32_t ts = tmem + lb + C::kTmS + cb, tp = tmem + lb + C::kTmP + cb;
+        const uint32_t ts = tmem + lb + kTmSq + (t & 1) * kBlk + cb, tp = tmem + lb + kTmPq + cb;
         tmem_ld32x4(ts, ts + 32, tp, tp + 32, s0, s1, d0, d1);
+        // dP(t) is in registers: the MMA warp may compute dP(t+1) over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v.dp_free);
         // masked only on the diagonal block (causal) and a ragged last block
         const bool masked = (CAUSAL && t == ib) || k0 + kBlk > N;
         if (masked)
@@ -594,7 +661,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
 #pragma unroll 1
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {  // half the columns
             uint32_t a[32], pa[16];
-            tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
+            tmem_ld32(tmem + lb + kTmAccq + 32 * c, a);
 #pragma unroll
             for (int t = 0; t < 16; ++t)
                 pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale,
@@ -617,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<D>;
     const View<D> v = view<D>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.s_full, v.p_full, v.o_full,
-                                         v.abort_flag, C::kStages);
+    if (threadIdx.x == 0) setup_barriers(v.once, v.full, v.empty, v.vfull, v.vempty, v.s_full, v.p_full,
+                                         v.o_full, v.dp_free,
+                                         v.abort_flag);
     if (warp == kMmaWarp) {
         tmem_alloc(v.tmem_slot, kTmemCols);
         tmem_relinquish();
