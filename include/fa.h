@@ -37,7 +37,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_NULL = -1,        /* a required pointer is NULL */
     FA_ERR_SHAPE = -2,       /* B, H or N < 1, or a size overflows the indexing */
-    FA_ERR_HEADDIM = -3,     /* d is not 64 or 128 */
+    FA_ERR_HEADDIM = -3,     /* d not supported by the entry point (see each) */
     FA_ERR_ALIGN = -4,       /* Q, K, V, O not 16-byte aligned, or LSE not 4-byte */
     FA_ERR_ARCH = -5,        /* current device is not compute capability 10.3 */
     FA_ERR_LAUNCH = -6,      /* a CUDA call failed (launch, copy, tensor map) */
@@ -57,7 +57,9 @@ typedef enum {
  *   LSE      fp32 [B, H, N], device memory, written: log(sum_j exp(s_ij))
  *            over the scaled, masked scores s_ij = scale * q_i . k_j.
  *   B, H, N  >= 1.  B*H < 2^31, N < 2^31.
- *   d        64 or 128 (head dimension; values have the same width).
+ *   d        64, 128 or 256 (head dimension; values have the same width;
+ *            the pages list all three).  At 256 a separate kernel runs:
+ *            128 query rows per work item, with S double-buffered in TMEM.
  *   causal   0: every key; nonzero: key j is used for query i iff j <= i.
  *   scale    finite, > 0; the pages' choice is 1/sqrt(d).
  *
@@ -137,6 +139,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                   the same Q, K, V, causal and scale), device, read
  *   LSE             fp32 [B, H, N], device, read
  *   dQ, dK, dV      bf16 [B, H, N, d], device, written
+ *   d               64 or 128 (FA_ERR_HEADDIM for 256: the forward only)
  *   workspace       caller-owned device scratch of at least
  *                   fa_bwd_workspace_bytes(B, H, N, d) bytes, 256-byte aligned
  * Three kernels on `stream` (D, then dK/dV with key blocks outermost, then

@@ -57,14 +57,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost).  Box = 64 columns
 // (128 bytes, the 128-byte swizzle span) x 128 rows x 1 head.  Rows past N
 // inside a head read as zero, so a ragged tail never touches the next head.
-bool encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+bool encode_qkv_map(CUtensorMap *m, const void *base, int BH, int N, int d, int rows = 128) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                    static_cast<cuuint64_t>(N) * d * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -98,9 +98,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Shape and scalar checks shared by both entry points.
-int check_shape(int B, int H, int N, int d, float scale) {
+// `fwd`: the forward entry points, which also take d = 256.
+int check_shape(int B, int H, int N, int d, float scale, bool fwd = false) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && !(fwd && d == 256)) return FA_ERR_HEADDIM;
     if (static_cast<long long>(B) * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
     const long long qblocks = (static_cast<long long>(N) + 255) / 256;
     if (qblocks * B * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;  // grid size
@@ -129,7 +130,7 @@ extern "C" {
 int fa_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                int H, int H_kv, int N, int d, int causal, float scale, fa_stream_t stream) {
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
-    int rc = check_shape(B, H, N, d, scale);
+    int rc = check_shape(B, H, N, d, scale, true);
     if (rc != FA_OK) return rc;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
     const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -147,14 +148,16 @@ int fa_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE,
 
     rc = check_arch();
     if (rc != FA_OK) return rc;
-    CUtensorMap tmQ, tmK, tmV;
+    CUtensorMap tmQ, tmK, tmV, tmV64;
     if (!encode_qkv_map(&tmQ, Q, B * H, N, d) || !encode_qkv_map(&tmK, K, B * H_kv, N, d) ||
-        !encode_qkv_map(&tmV, V, B * H_kv, N, d))
+        !encode_qkv_map(&tmV, V, B * H_kv, N, d) ||
+        (d == 256 && !encode_qkv_map(&tmV64, V, B * H_kv, N, d, 64)))
         return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     fa::LaunchArgs a;
     a.tmQ = &tmQ;
     a.tmK = &tmK;
     a.tmV = &tmV;
+    a.tmV64 = d == 256 ? &tmV64 : nullptr;
     a.O = O;
     a.LSE = LSE;
     a.BH = B * H;
@@ -175,7 +178,7 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int
 }
 
 size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
-    if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
+    if (check_shape(B, H, N, d, 1.f, true) != FA_OK) return 0;
     const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
     const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
     return 4 * align256(t_bytes) + align256(l_bytes);
@@ -185,7 +188,7 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
                 float *LSE_host, void *workspace, size_t workspace_bytes, int B, int H, int N,
                 int d, int causal, float scale, fa_stream_t stream) {
     if (!Q_host || !K_host || !V_host || !O_host || !LSE_host) return FA_ERR_NULL;
-    int rc = check_shape(B, H, N, d, scale);
+    int rc = check_shape(B, H, N, d, scale, true);
     if (rc != FA_OK) return rc;
     const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
     if (!workspace || workspace_bytes < need ||
@@ -377,14 +380,16 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
 }
 
 int fa_device_error(fa_stream_t stream) {
-    int v = 0, vb = 0, vd = 0;
+    int v = 0, vb = 0, vd = 0, v2 = 0;
     int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
     if (rc != FA_OK) return rc;
     rc = fa::bwd_read_and_clear_status(&vb);
     if (rc != FA_OK) return rc;
     rc = fa::dec_read_and_clear_status(&vd);
     if (rc != FA_OK) return rc;
-    return (v == 0 && vb == 0 && vd == 0) ? FA_OK : FA_ERR_TIMEOUT;
+    rc = fa::fwd256_read_and_clear_status(&v2);
+    if (rc != FA_OK) return rc;
+    return (v == 0 && vb == 0 && vd == 0 && v2 == 0) ? FA_OK : FA_ERR_TIMEOUT;
 }
 
 int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {

@@ -674,6 +674,7 @@ static int launch_t(const LaunchArgs &a) {
 int launch_fwd(const LaunchArgs &a) {
     if (a.d == 64) return a.causal ? launch_t<64, true>(a) : launch_t<64, false>(a);
     if (a.d == 128) return a.causal ? launch_t<128, true>(a) : launch_t<128, false>(a);
+    if (a.d == 256) return launch_fwd256(a);
     return FA_ERR_HEADDIM;
 }
 

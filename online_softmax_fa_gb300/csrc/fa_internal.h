@@ -13,6 +13,7 @@ namespace fa {
 
 struct LaunchArgs {
     const CUtensorMap *tmQ, *tmK, *tmV;
+    const CUtensorMap *tmV64;  // d = 256: V with 64-row boxes
     void *O;
     float *LSE;
     int BH, N, d;
@@ -24,6 +25,9 @@ struct LaunchArgs {
 };
 
 int launch_fwd(const LaunchArgs &a);
+// d = 256 forward (fa_fwd256_sm103.cu).
+int launch_fwd256(const LaunchArgs &a);
+int fwd256_read_and_clear_status(int *status);
 
 // Backward pass (fa_bwd_sm103.cu).
 struct BwdArgs {

@@ -74,6 +74,8 @@ WORKLOADS = {
     "long": Workload("long", 1, 8, 32771, 128, (True,), 5, sampled_rows=512),
     # Llama-3-8B's own head layout: 32 query heads share 8 K/V heads
     "llama_gqa": Workload("llama_gqa", 1, 32, 8192, 128, (True,), 6, H_kv=8),
+    # head dimension 256 at the llama workload's FLOP count (16 heads x 256)
+    "d256": Workload("d256", 1, 16, 8192, 256, (True,), 8),
 }
 
 # Decoding: one new query row per (sequence, head) against a K/V cache of N

@@ -72,7 +72,7 @@ def test_late_max_workload(fa, causal):
 EDGE_N = [1, 2, 63, 127, 128, 129, 255, 256, 257, 300, 383, 512, 640, 1000]
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", EDGE_N)
 def test_edge_sweep(fa, N, d, causal):
@@ -101,6 +101,43 @@ def test_batch_and_heads_layout(fa):
         o, lse = run(fa, q, k, v, causal, scale_of(128))
         O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale_of(128))
         check(o, lse, O_ref, L_ref, f"layout causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256_layout_and_late_max(fa, causal):
+    """d = 256 (its own kernel): B, H > 1, ragged N, and keys whose scores
+    grow along the row, so the reference max moves and O is rescaled."""
+    q, k, v = make_qkv(2, 3, 777, 256, seed=31, k_row_ramp=True)
+    o, lse = run(fa, q, k, v, causal, scale_of(256))
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale_of(256))
+    check(o, lse, O_ref, L_ref, f"d256 late causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.3])
+def test_head_dim_256_large_scores(fa, scale):
+    q, k, v = make_qkv(1, 2, 640, 256, seed=33)
+    q = (q.float() * 2).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = run(fa, q, k, v, causal, scale)
+        O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale)
+        check(o, lse, O_ref, L_ref, f"d256 scale={scale} causal={causal}")
+
+
+def test_head_dim_256_workload_sampled(fa):
+    _sampled_check(fa, WORKLOADS["d256"], 24, True)
+
+
+def test_head_dim_256_gqa(fa):
+    q, k, v = make_qkv(2, 8, 600, 256, seed=35, H_kv=2)
+    dev = torch.device("cuda")
+    for causal in (False, True):
+        o, lse = fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), causal=causal,
+                               scale=scale_of(256))
+        torch.cuda.synchronize()
+        assert fa.fa_device_error() == 0
+        O_ref, L_ref = oracle.attention_fwd_gqa(q, k, v, causal=causal, scale=scale_of(256))
+        check(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref,
+              f"d256 gqa causal={causal}")
 
 
 # ------------------------------------------------------------ closed forms
