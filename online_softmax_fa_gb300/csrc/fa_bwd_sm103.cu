@@ -26,9 +26,10 @@
 //           and dP run on the tensor pipe while the warps work on this one.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
 // is masked.  TMEM (dkdv): S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d, 256+2d); P^T and dS^T are bf16 pairs over columns [0,32) and
-// [64,96) of S^T and dP^T (each column-half warp writes over its own first
-// 32 columns).  TMEM (dq): S [0,128) and [128,256), dP [256,384),
+// dK [256+d, 256+2d); P^T and dS^T are bf16 pairs in the S^T region, over
+// columns [0,32) / [64,96) and [32,64) / [96,128) (each column-half warp
+// writes over its own 64 columns), so dP^T of the next block can be computed
+// while they wait for dV / dK.  TMEM (dq): S [0,128) and [128,256), dP [256,384),
 // dQ [384,384+d).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -155,13 +156,14 @@ __device__ __forceinline__ void mma_rows_rows(uint32_t d_tm, uint64_t da, uint64
 
 // acc[M128 x N(D)] (+)= A[tmem, 128 x 128 bf16] * B[128 rows x D, MN-major].
 // A's bf16 pairs sit in two column groups (written by the two column-half
-// warps over their own fp32 columns): K-steps 0-3 at columns [0, 32), 4-7
-// at [64, 96) of the region.
+// warps over their own fp32 columns): K-steps 0-3 at columns [a_off,
+// a_off + 32), 4-7 at [64 + a_off, 96 + a_off) of the region.
 template <int D>
-__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tm, uint32_t a_tm, uint64_t db, bool acc) {
+__device__ __forceinline__ void mma_tmem_rows(uint32_t d_tm, uint32_t a_tm, uint64_t db, bool acc,
+                                              uint32_t a_off = 0) {
 #pragma unroll
     for (int kk = 0; kk < kBlk / 16; ++kk)
-        mma_ts_elect(d_tm, a_tm + (kk >> 2) * 64 + (kk & 3) * 8,
+        mma_ts_elect(d_tm, a_tm + (kk >> 2) * 64 + a_off + (kk & 3) * 8,
                      db + static_cast<uint64_t>((kk * 16 * 128) >> 4), Cfg<D>::kIdescAcc,
                      (acc || kk > 0) ? 1u : 0u);
 }
@@ -262,6 +264,19 @@ __device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint3
     }
 }
 
+// Non-blocking test of a barrier phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_ready(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // ============================== dK / dV kernel ==============================
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUtensorMap *tmK,
@@ -331,24 +346,54 @@ __device__ __forceinline__ void dkdv_mma(const Params &p) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
+    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+    const auto so_of = [](int t) {
+        return static_cast<uint64_t>(((t % C::kStages) * 2 * C::kTile) >> 4);
+    };
+    // P^T and dS^T both land in the S^T region, so the dP^T region is free
+    // as soon as the elementwise warps have read it (dp_free): dP^T of the
+    // next block is issued then when its dO has already arrived (tested
+    // without blocking), else after dV / dK.  S^T of the next block follows
+    // dV / dK (which read P^T and dS^T from its region).
     bool ok = wait(v.once, 0, kSiteKV);
-    if (ok) tc_fence_after();
-    for (int t = 0; t < n_q && ok; ++t) {
-        const int s = t % C::kStages;
-        ok = wait(&v.full[s], (t / C::kStages) & 1, kSiteQ);
-        if (!ok) break;
+    if (ok) ok = wait(&v.full[0], 0, kSiteQ);
+    if (ok) {
         tc_fence_after();
-        const uint64_t so = static_cast<uint64_t>((s * 2 * C::kTile) >> 4);
-        const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
-        mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so);        // S^T = K Q^T
-        mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so + to);   // dP^T = V dO^T
+        mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k);       // S^T(0) = K Q_0^T
+        mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + to);  // dP^T(0) = V dO_0^T
         mma_commit_elect(v.s_full);
+    }
+    for (int t = 0; t < n_q && ok; ++t) {
+        const int t1 = t + 1;
+        const bool more = t1 < n_q;
+        bool early = false;
+        if (more) {
+            ok = wait(v.dp_free, t & 1, kSiteP);
+            if (!ok) break;
+            early = __all_sync(0xffffffffu,
+                               mbar_ready(&v.full[t1 % C::kStages], (t1 / C::kStages) & 1));
+            if (early) {
+                tc_fence_after();
+                mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so_of(t1) + to);  // dP^T(t+1)
+            }
+        }
         ok = wait(v.p_full, t & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
-        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0);  // dV
-        mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmP, ring_mn + so, t > 0);       // dK
-        mma_commit_elect(&v.empty[s]);
+        const uint64_t so = so_of(t);
+        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0, 0);  // dV
+        mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmS, ring_mn + so, t > 0, 32);      // dK
+        mma_commit_elect(&v.empty[t % C::kStages]);
+        if (more) {
+            if (!early) {
+                ok = wait(&v.full[t1 % C::kStages], (t1 / C::kStages) & 1, kSiteQ);
+                if (!ok) break;
+                tc_fence_after();
+                mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so_of(t1) + to);  // dP^T(t+1)
+            }
+            mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so_of(t1));  // S^T(t+1)
+            mma_commit_elect(v.s_full);
+        }
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
@@ -392,6 +437,10 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
         uint32_t s0[32], s1[32], d0[32], d1[32], pp[16], pds[16];
         const uint32_t ts = tmem + lb + C::kTmS + cb, tp = tmem + lb + C::kTmP + cb;
         tmem_ld32x4(ts, ts + 32, tp, tp + 32, s0, s1, d0, d1);
+        // dP^T is in registers: the MMA warp may compute the next one over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(v.dp_free);
         // masked only on the diagonal block (causal) and a ragged last block
         const bool masked = (CAUSAL && t == 0) || q0 + kBlk > N;
         if (masked)
@@ -399,8 +448,10 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
                         lim_hi, cb, pp, pds);
         else
             p_ds_fast(s0, d0, lse2 + cb, dd + cb, true, 0.f, 0.f, p.scale_log2, pp, pds);
+        // P^T over the first 32 columns of this warp's S^T slice, dS^T over
+        // the next 32
         tmem_st16(ts, pp);
-        tmem_st16(tp, pds);
+        tmem_st16(ts + 32, pds);
         if (masked)
             p_ds_masked(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2,
                         lim_lo, lim_hi, cb + 32, pp, pds);
@@ -408,7 +459,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
             p_ds_fast(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2, pp,
                       pds);
         tmem_st16(ts + 16, pp);
-        tmem_st16(tp + 16, pds);
+        tmem_st16(ts + 48, pds);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
