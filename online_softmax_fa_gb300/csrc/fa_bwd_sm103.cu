@@ -770,34 +770,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Per query row, into rows padded to Npad (a multiple of 128) per head, so
 // that the other kernels fetch a block's rows with aligned bulk copies:
 // -D = -rowsum(dO * O) (fp32) and -LSE * log2(e); zeros for rows past N.
-// One warp per padded row.
+// D/8 lanes per row, one 16-byte load of O and of dO each (32 / (D/8) rows
+// per warp).
 template <int D>
 __global__ void pre_kernel(const __nv_bfloat16 *__restrict__ O,
                            const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ LSE,
                            float *__restrict__ lse2, float *__restrict__ dd, int N, int Npad,
                            long long rows_pad) {
-    constexpr int E = D / 32;
+    constexpr int LPR = D / 8;        // lanes per row
+    constexpr int RPW = 32 / LPR;     // rows per warp
     const int lane = threadIdx.x & 31;
-    for (long long prow = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-         prow < rows_pad; prow += static_cast<long long>(gridDim.x) * 4) {
+    const int sub = lane / LPR, c = lane % LPR;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long wr = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         wr * RPW < rows_pad; wr += warps) {
+        const long long prow = wr * RPW + sub;  // rows_pad is a multiple of 128: in range
         const long long bh = prow / Npad;
         const int q = static_cast<int>(prow - bh * Npad);
-        float acc = 0.f, l2 = 0.f;
+        float acc = 0.f;
         if (q < N) {
             const long long row = bh * N + q;
-            const __nv_bfloat16 *o = O + row * D + lane * E;
-            const __nv_bfloat16 *g = dO + row * D + lane * E;
+            const uint4 o4 = *reinterpret_cast<const uint4 *>(O + row * D + c * 8);
+            const uint4 g4 = *reinterpret_cast<const uint4 *>(dO + row * D + c * 8);
+            const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            l2 = LSE[row] * kLog2e;
+            for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
+                acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u),
+                           __uint_as_float(gw[e] & 0xFFFF0000u), acc);
+            }
         }
-        if (lane == 0) {
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (c == 0) {
             dd[prow] = -acc;
-            lse2[prow] = -l2;
+            lse2[prow] = q < N ? -LSE[bh * N + q] * kLog2e : 0.f;
         }
     }
 }
@@ -824,7 +831,7 @@ static int launch_bwd_t(const BwdArgs &a) {
     const int Npad = n_blocks * bwd::kBlk;
     const long long rows_pad = static_cast<long long>(a.BH) * Npad;
     float *lse2 = a.rows, *dd = a.rows + rows_pad;
-    const long long pre_blocks = (rows_pad + 3) / 4;
+    const long long pre_blocks = (rows_pad / (32 / (D / 8)) + 3) / 4;  // 4 warps per block
     bwd::pre_kernel<D><<<static_cast<unsigned>(pre_blocks < (1 << 20) ? pre_blocks : (1 << 20)),
                          128, 0, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.O), static_cast<const __nv_bfloat16 *>(a.dO),
