@@ -101,10 +101,14 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * fa_fwd_host -- the same operation on HOST buffers: copies Q, K, V from
- * host to the device workspace, runs fa_fwd, and copies O and LSE back, all
- * enqueued on `stream` (asynchronous; synchronise the stream before reading
- * O_host / LSE_host).  Host buffers should be pinned for the copies to
- * overlap; pageable memory works but the copies then block the host.
+ * host to the device workspace, runs fa_fwd, and copies O and LSE back,
+ * asynchronously with respect to the host and ordered after the earlier work
+ * on `stream` (synchronise `stream` before reading O_host / LSE_host).  The
+ * heads are cut into chunks whose copy-in, kernel and copy-out overlap on
+ * three streams the library creates once per device (and keeps); calls that
+ * use them are enqueued one at a time.  The results equal those of one
+ * fa_fwd call.  Host buffers should be pinned for the copies to overlap;
+ * pageable memory works but the copies then block the host.
  *
  *   Q_host, K_host, V_host  bf16 [B, H, N, d] in host memory (read).
  *   O_host                  bf16 [B, H, N, d] in host memory (written).

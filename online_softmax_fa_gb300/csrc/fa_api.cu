@@ -184,6 +184,38 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
     return 4 * align256(t_bytes) + align256(l_bytes);
 }
 
+namespace {
+// Streams and events of the host-buffer path, created once per device and
+// kept for the life of the process; `mu` serialises the enqueueing of calls
+// that share them.
+struct HostPipe {
+    static constexpr int kMaxChunks = 8;
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
+};
+HostPipe g_pipes[64];
+
+// Creates the device's streams and events on first use; call with h.mu held.
+int host_pipe_init(HostPipe &h) {
+    if (h.ready) return FA_OK;
+    const unsigned fl = cudaStreamNonBlocking;
+    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.in, fl));
+    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.comp, fl));
+    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.out, fl));
+    FA_CUDA_TRY(cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming));
+    FA_CUDA_TRY(cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming));
+    for (int c = 0; c < HostPipe::kMaxChunks; ++c) {
+        FA_CUDA_TRY(cudaEventCreateWithFlags(&h.loaded[c], cudaEventDisableTiming));
+        FA_CUDA_TRY(cudaEventCreateWithFlags(&h.computed[c], cudaEventDisableTiming));
+    }
+    h.ready = true;
+    return FA_OK;
+}
+}  // namespace
+
 int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
                 float *LSE_host, void *workspace, size_t workspace_bytes, int B, int H, int N,
                 int d, int causal, float scale, fa_stream_t stream) {
@@ -197,19 +229,71 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
     rc = check_arch();
     if (rc != FA_OK) return rc;
     const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
-    const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
     uint8_t *w = static_cast<uint8_t *>(workspace);
     uint8_t *dQ = w, *dK = dQ + align256(t_bytes), *dV = dK + align256(t_bytes);
     uint8_t *dO = dV + align256(t_bytes);
     float *dL = reinterpret_cast<float *>(dO + align256(t_bytes));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    FA_CUDA_TRY(cudaMemcpyAsync(dQ, Q_host, t_bytes, cudaMemcpyHostToDevice, s));
-    FA_CUDA_TRY(cudaMemcpyAsync(dK, K_host, t_bytes, cudaMemcpyHostToDevice, s));
-    FA_CUDA_TRY(cudaMemcpyAsync(dV, V_host, t_bytes, cudaMemcpyHostToDevice, s));
-    rc = fa_fwd(dQ, dK, dV, dO, dL, B, H, N, d, causal, scale, stream);
+
+    // The heads are independent, so the work is cut into chunks of heads:
+    // the copy-in of chunk c+1, the kernel on chunk c and the copy-out of
+    // chunk c-1 overlap on three streams.  Each chunk keeps at least about
+    // one query block per SM, so the kernel stays reasonably efficient while
+    // the copies (the longer part) hide it; the results are those of one
+    // fa_fwd call (each head is computed the same way).
+    int dev = 0;
+    FA_CUDA_TRY(cudaGetDevice(&dev));
+    int sms = 0;
+    FA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const long long BH = static_cast<long long>(B) * H;
+    const long long rows_per_item = d == 256 ? 128 : 256;
+    const long long qblocks = (static_cast<long long>(N) + rows_per_item - 1) / rows_per_item;
+    long long chunks = BH * qblocks / (sms > 0 ? sms : 1);
+    if (chunks > HostPipe::kMaxChunks) chunks = HostPipe::kMaxChunks;
+    if (chunks > BH) chunks = BH;
+    if (chunks < 1) chunks = 1;
+    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
+    HostPipe *hp = &g_pipes[dev];
+    std::lock_guard<std::mutex> lock(hp->mu);
+    rc = host_pipe_init(*hp);
     if (rc != FA_OK) return rc;
-    FA_CUDA_TRY(cudaMemcpyAsync(O_host, dO, t_bytes, cudaMemcpyDeviceToHost, s));
-    FA_CUDA_TRY(cudaMemcpyAsync(LSE_host, dL, l_bytes, cudaMemcpyDeviceToHost, s));
+    // everything below runs after the caller's earlier work on `stream`
+    FA_CUDA_TRY(cudaEventRecord(hp->start, s));
+    FA_CUDA_TRY(cudaStreamWaitEvent(hp->in, hp->start, 0));
+    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp, hp->start, 0));
+    FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->start, 0));
+    const size_t head_t = static_cast<size_t>(N) * d * 2, head_l = static_cast<size_t>(N) * 4;
+    for (long long c = 0; c < chunks; ++c) {
+        const long long h0 = c * BH / chunks, h1 = (c + 1) * BH / chunks;
+        const size_t off_t = h0 * head_t, n_t = (h1 - h0) * head_t;
+        const size_t off_l = h0 * head_l, n_l = (h1 - h0) * head_l;
+        FA_CUDA_TRY(cudaMemcpyAsync(dQ + off_t, static_cast<const uint8_t *>(Q_host) + off_t, n_t,
+                                    cudaMemcpyHostToDevice, hp->in));
+        FA_CUDA_TRY(cudaMemcpyAsync(dK + off_t, static_cast<const uint8_t *>(K_host) + off_t, n_t,
+                                    cudaMemcpyHostToDevice, hp->in));
+        FA_CUDA_TRY(cudaMemcpyAsync(dV + off_t, static_cast<const uint8_t *>(V_host) + off_t, n_t,
+                                    cudaMemcpyHostToDevice, hp->in));
+        FA_CUDA_TRY(cudaEventRecord(hp->loaded[c], hp->in));
+        FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp, hp->loaded[c], 0));
+        // one batch of h1 - h0 heads (B = 1): MHA heads need no batch index
+        rc = fa_fwd(dQ + off_t, dK + off_t, dV + off_t, dO + off_t,
+                    reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dL) + off_l), 1,
+                    static_cast<int>(h1 - h0), N, d, causal, scale,
+                    reinterpret_cast<fa_stream_t>(hp->comp));
+        if (rc != FA_OK) return rc;
+        FA_CUDA_TRY(cudaEventRecord(hp->computed[c], hp->comp));
+        FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->computed[c], 0));
+        FA_CUDA_TRY(cudaMemcpyAsync(static_cast<uint8_t *>(O_host) + off_t, dO + off_t, n_t,
+                                    cudaMemcpyDeviceToHost, hp->out));
+        FA_CUDA_TRY(cudaMemcpyAsync(reinterpret_cast<uint8_t *>(LSE_host) + off_l,
+                                    reinterpret_cast<uint8_t *>(dL) + off_l, n_l,
+                                    cudaMemcpyDeviceToHost, hp->out));
+    }
+    // the caller's stream resumes once the last copy-out is done (the
+    // copy-out stream has waited for every kernel, which waited for every
+    // copy-in)
+    FA_CUDA_TRY(cudaEventRecord(hp->done, hp->out));
+    FA_CUDA_TRY(cudaStreamWaitEvent(s, hp->done, 0));
     return FA_OK;
 }
 

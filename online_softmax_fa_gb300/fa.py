@@ -152,10 +152,12 @@ def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, workspace,
                 causal: bool = False, scale: float | None = None, stream=None):
-    """Host-buffer variant: H2D copies, the kernel and D2H copies, all
-    enqueued on one stream.  Tensors are CPU (ideally pinned); ``workspace``
-    is a CUDA uint8 tensor of at least fa_fwd_host_workspace_bytes bytes.
-    Asynchronous: synchronise the stream before reading o_host/lse_host."""
+    """Host-buffer variant: H2D copies, the kernel and D2H copies, overlapped
+    across chunks of heads on the library's own streams and ordered after the
+    work already on ``stream``.  Tensors are CPU (ideally pinned);
+    ``workspace`` is a CUDA uint8 tensor of at least
+    fa_fwd_host_workspace_bytes bytes.  Asynchronous: synchronise the stream
+    before reading o_host/lse_host."""
     B, H, N, d = (int(x) for x in q_host.shape)
     if scale is None:
         scale = 1.0 / math.sqrt(d)

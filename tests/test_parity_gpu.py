@@ -241,6 +241,24 @@ def test_bounded_wait_expires_with_status(fa):
     check(o, lse, O_ref, L_ref, "after selftest")
 
 
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 40, 2048, 64, True), (1, 100, 8192, 64, False),
+                                         (1, 20, 4096, 256, True)])
+def test_host_buffer_chunked_pipeline_is_bit_identical(fa, B, H, N, d, causal):
+    """Shapes that the host path cuts into several (uneven) chunks of heads:
+    the outputs must equal one fa_fwd call on device buffers, bit for bit."""
+    q, k, v = make_qkv(B, H, N, d, seed=60 + H + d)
+    dev = torch.device("cuda")
+    o_ref, l_ref = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale_of(d))
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    fa.fa_fwd_host(qh, kh, vh, oh, lh, ws, causal=causal, scale=scale_of(d))
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
 # ------------------------------------------------- grouped-query attention
 @pytest.mark.parametrize("H,H_kv,N,d,causal", [
     (8, 2, 1000, 128, True), (8, 2, 1000, 128, False), (6, 1, 300, 64, True),
