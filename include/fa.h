@@ -179,7 +179,7 @@ size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int N, int d);
  *   LSE      fp32 [B, H]
  *   H_kv     divides H; H / H_kv in {1, 2, 4, 8} (FA_ERR_UNSUPPORTED else);
  *            each K/V row is read once for all query heads of its group
- *   d        64 or 128; B * H_kv <= 65535
+ *   d        64, 128 or 256; B * H_kv <= 65535
  *   workspace  caller-owned device memory of at least
  *            fa_decode_workspace_bytes(B, H, H_kv, N, d) bytes, 256-byte
  *            aligned; its contents are scratch and it must not overlap the

@@ -301,7 +301,7 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
 namespace {
 int check_decode_shape(int B, int H, int H_kv, int N, int d, float scale) {
     if (B < 1 || H < 1 || H_kv < 1 || N < 1) return FA_ERR_SHAPE;
-    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (H % H_kv != 0) return FA_ERR_SHAPE;
     const int G = H / H_kv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return FA_ERR_UNSUPPORTED;

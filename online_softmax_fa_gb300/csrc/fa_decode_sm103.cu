@@ -39,7 +39,9 @@
 namespace fa {
 
 constexpr int kDecWarps = 4;       // warps per CTA of the merge kernel
-constexpr int kDecTileKeys = 128;  // keys per K/V tile of the split kernel
+// keys per K/V tile of the split kernel: 128, or 64 at d = 256 (stage size)
+template <int D>
+constexpr int dec_tile_keys() { return D == 256 ? 64 : 128; }
 constexpr int kDecConsumers = 8;   // consumer warps per split CTA
 constexpr int kDecThreads = (kDecConsumers + 1) * 32;  // + one producer warp
 constexpr int kDecMaxGrid = 1024;
@@ -76,7 +78,7 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 __device__ int g_fa_status_dec;  // bounded-wait timeouts of the decoding kernels
 
 // ------------------------------------------------------------ work partition
-// The K/V cache is cut into tiles of kDecTileKeys keys; the tiles of all
+// The K/V cache is cut into tiles of dec_tile_keys<D>() keys; the tiles of all
 // (batch, K/V head) pairs form one sequence of T = heads * T_h tiles, and
 // CTA c of `grid` takes the contiguous run [c*T/grid, (c+1)*T/grid).  Every
 // CTA streams the same number of bytes (to one tile), and a run crosses at
@@ -104,10 +106,11 @@ struct DecCfg {
     static constexpr int kHeadsPerWarp = G < 4 ? G : 4;
     static constexpr int kHeadGroups = G / kHeadsPerWarp;
     static constexpr int kWarpsPerGroup = kDecConsumers / kHeadGroups;
-    static constexpr int kKeysPerWarp = kDecTileKeys / kWarpsPerGroup;  // per tile
+    static constexpr int kTileKeys = dec_tile_keys<D>();
+    static constexpr int kKeysPerWarp = kTileKeys / kWarpsPerGroup;  // per tile
     static constexpr int kSteps = kKeysPerWarp / kKeysPerStep;
-    static constexpr int kTileBytes = kDecTileKeys * D * 2;  // one K or V tile
-    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kTileBytes = kTileKeys * D * 2;  // one K or V tile
+    static constexpr int kStages = (D == 64) ? 6 : 3;
     static constexpr int kOffRing = 0;                       // [S][K tile, V tile]
     static constexpr int kOffRed = kStages * 2 * kTileBytes;  // merge scratch
     static constexpr int kRedFloats = kDecConsumers * kHeadsPerWarp * (D + 2);
@@ -179,9 +182,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (!ok) break;
             uint8_t *dst = smem + C::kOffRing + s * 2 * C::kTileBytes;
             mbar_arrive_expect_tx(&full[s], 2 * C::kTileBytes);
-            for (int r = 0; r < kDecTileKeys; r += 64) {  // 64-row boxes
-                tma_load_3d(dst + r * D * 2, &tmK, &full[s], 0, j * kDecTileKeys + r, h, pol);
-                tma_load_3d(dst + C::kTileBytes + r * D * 2, &tmV, &full[s], 0, j * kDecTileKeys + r, h, pol);
+            for (int r = 0; r < C::kTileKeys; r += 64) {  // 64-row boxes
+                tma_load_3d(dst + r * D * 2, &tmK, &full[s], 0, j * C::kTileKeys + r, h, pol);
+                tma_load_3d(dst + C::kTileBytes + r * D * 2, &tmV, &full[s], 0,
+                            j * C::kTileKeys + r, h, pol);
             }
         }
         // every copy issued lands before the CTA exits (bounded)
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
             for (int st = 0; st < SG; ++st) {
                 const int kk = wg * C::kKeysPerWarp + (st0 + st) * KPS + sub;  // key in tile
-                valid[st] = j * kDecTileKeys + kk < N;
+                valid[st] = j * C::kTileKeys + kk < N;
                 kt[st] = lds128(kt_s + kk * (D * 2) + cw * 16);
                 vt[st] = lds128(vt_s + kk * (D * 2) + cw * 16);
             }
@@ -503,7 +507,7 @@ static int launch_decode_t(const DecodeArgs &a) {
     const int sms = dec_sm_count(dev);
     if (sms <= 0) return record_message(FA_ERR_LAUNCH, "cannot query the SM count");
     const int heads = a.B * a.H_kv;
-    const int T_h = (a.N + kDecTileKeys - 1) / kDecTileKeys;
+    const int T_h = (a.N + C::kTileKeys - 1) / C::kTileKeys;
     const long long T = static_cast<long long>(heads) * T_h;
     int grid = sms < kDecMaxGrid ? sms : kDecMaxGrid;
     if (T < grid) grid = static_cast<int>(T);
@@ -534,6 +538,7 @@ static int launch_decode_d(const DecodeArgs &a) {
 
 int launch_decode(const DecodeArgs &a) {
     if (a.d == 64) return launch_decode_d<64>(a);
+    if (a.d == 256) return launch_decode_d<256>(a);
     if (a.d == 128) return launch_decode_d<128>(a);
     return FA_ERR_HEADDIM;
 }

@@ -316,7 +316,7 @@ def _decode_check(fa, q, k, v, scale, what):
 
 
 @pytest.mark.parametrize("N", [1, 7, 63, 64, 65, 1000, 4097])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("H,H_kv", [(8, 8), (8, 4), (8, 2), (8, 1)])
 def test_decode_parity(fa, N, d, H, H_kv):
     q, k, v = make_decode(2, H, H_kv, N, d, seed=60 + N + H_kv)
