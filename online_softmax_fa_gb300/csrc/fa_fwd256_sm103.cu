@@ -345,28 +345,34 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
             if (!ok) break;
             tc_fence_after();
             const uint32_t tm_s = tmem + lane_bits + kTmS + (t & 1) * kBlockN;
+            // S row and its max over the tile in one TMEM load (the load's
+            // max reduction)
             uint32_t raw[128];
-            tmem_ld128(tm_s, raw);
+            float mx;
+            tmem_ld128_max(tm_s, raw, mx);
             float *sv = reinterpret_cast<float *>(raw);
             const int key0 = j * kBlockN;
             const bool ragged = key0 + kBlockN > N;
             const bool diag = CAUSAL && (key0 + kBlockN - 1 > w.qb * kBlockM);
-            if (ragged || diag) {  // keys past N or above the diagonal -> -inf
+            if (ragged || diag) {
+                // keys past N or above the diagonal -> -inf, and the row max
+                // over the remaining keys only (columns 0-15, then 16 more
+                // per step)
                 int lim = N - key0;
                 if (CAUSAL) lim = min(lim, qrow - key0 + 1);
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) sv[c] = -INFINITY;
+                float pm[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pm[e] = fmaxf(sv[e], sv[8 + e]);
+#pragma unroll
+                for (int c = 16; c + 16 <= kBlockN; c += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) pm[e] = fmax3(pm[e], sv[c + e], sv[c + 8 + e]);
+                mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
+                           fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             }
-            float pm[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) pm[e] = fmax3(sv[e], sv[8 + e], sv[16 + e]);
-#pragma unroll
-            for (int c = 24; c + 16 <= kBlockN; c += 16)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) pm[e] = fmax3(pm[e], sv[c + e], sv[c + 8 + e]);
-            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
-                                   fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const float cand = mx * cs;
             const float m_new = (cand > m + kStaleMax) ? cand : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;

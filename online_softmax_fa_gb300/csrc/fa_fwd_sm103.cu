@@ -439,30 +439,36 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
             if (!ok) break;
             ++sc;
             tc_fence_after();
+            // S row and its max over the tile in one TMEM load (the load's
+            // max reduction)
             uint32_t raw[128];
-            tmem_ld128(tm_s, raw);
+            float mx;
+            tmem_ld128_max(tm_s, raw, mx);
             float *sv = reinterpret_cast<float *>(raw);
 
             const int key0 = j * kBlockN;
             const bool ragged = key0 + kBlockN > N;
             const bool diag = CAUSAL && (key0 + kBlockN - 1 > sub_start);
-            if (ragged || diag) {  // keys past N or above the diagonal -> -inf
+            if (ragged || diag) {
+                // keys past N or above the diagonal -> -inf, and the row max
+                // over the remaining keys only: eight short chains of
+                // three-input max over all kBlockN columns (0-15, then 16
+                // more per step)
                 int lim = N - key0;
                 if (CAUSAL) lim = min(lim, qrow - key0 + 1);
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= lim) sv[c] = -INFINITY;
+                float pm[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) pm[t] = fmaxf(sv[t], sv[8 + t]);
+#pragma unroll
+                for (int c = 16; c + 16 <= kBlockN; c += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) pm[t] = fmax3(pm[t], sv[c + t], sv[c + 8 + t]);
+                mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
+                           fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             }
-            // Row max: eight short chains of three-input max.
-            float pm[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) pm[t] = fmax3(sv[t], sv[8 + t], sv[16 + t]);
-#pragma unroll
-            for (int c = 24; c + 16 <= kBlockN; c += 16)
-#pragma unroll
-                for (int t = 0; t < 8; ++t) pm[t] = fmax3(pm[t], sv[c + t], sv[c + 8 + t]);
-            const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
-                                   fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const float cand = mx * cs;
             const float m_new = (cand > m + kStaleMax) ? cand : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;

@@ -140,6 +140,45 @@ def test_head_dim_256_gqa(fa):
               f"d256 gqa causal={causal}")
 
 
+# ----------------------------------------------- one dominant key per row
+# Column positions that a 128-key tile (64 at d = 256 in decoding) treats
+# differently: first and last key, the edges of 8-, 16- and 64-key groups,
+# the last eight keys of a tile, and keys of later tiles.
+SPIKE_COLS = [0, 5, 15, 16, 63, 64, 119, 120, 121, 127, 128, 250, 255, 383]
+
+
+def _spike(q_rows, k, h_kv, col, scale, margin=150.0):
+    """Make key ``col`` of K/V head ``h_kv`` score ``margin`` (natural-log
+    units) for a query direction u = mean of ``q_rows``: k_col = alpha * u
+    with alpha * scale * |u|^2 = margin.  Every other score stays O(1), so
+    the running reference max must take this key, or exp of the gap
+    overflows fp32."""
+    u = q_rows.reshape(-1, q_rows.shape[-1]).mean(dim=0)
+    alpha = margin / (scale * float(u @ u))
+    k[:, h_kv, col] = alpha * u
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dominant_key_anywhere_in_a_tile(fa, d, causal):
+    H, N = len(SPIKE_COLS), 384
+    q, k, v = make_qkv(1, H, N, d, seed=90 + d)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(91 + d)
+    u = torch.randn(H, d, generator=g, dtype=torch.float32)
+    qf = u.view(1, H, 1, d) + 0.1 * q.float()  # every row of head h near u_h
+    kf = k.float()
+    scale = scale_of(d)
+    for h, c in enumerate(SPIKE_COLS):
+        _spike(qf[:, h], kf, h, c, scale)
+    q, k = qf.to(torch.bfloat16), kf.to(torch.bfloat16)
+    o, lse = run(fa, q, k, v, causal, scale)
+    O_ref, L_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=scale)
+    # rows that see their head's dominant key return (nearly) its value row
+    assert L_ref[0, 0, -1] > 100
+    check(o, lse, O_ref, L_ref, f"dominant key d={d} causal={causal}")
+
+
 # ------------------------------------------------------------ closed forms
 def test_closed_forms(fa):
     dev = torch.device("cuda")
@@ -349,6 +388,18 @@ def test_decode_matches_forward_last_row(fa):
     torch.cuda.synchronize()
     assert (o_f[:, :, -1].float() - o_d.float()).abs().max().item() <= 2 * O_MAX
     assert (l_f[:, :, -1] - l_d).abs().max().item() <= 2 * LSE_MAX
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_decode_dominant_key_anywhere_in_a_tile(fa, d):
+    cols = [0, 15, 16, 31, 32, 63, 64, 120, 127, 128, 1000, 4095, 4096]
+    H = len(cols)
+    q, k, v = make_decode(1, H, H, 4097, d, seed=92 + d)
+    kf = k.float()
+    scale = scale_of(d)
+    for h, c in enumerate(cols):
+        _spike(q[:, h].float(), kf, h, c, scale)
+    _decode_check(fa, q, kf.to(torch.bfloat16), v, scale, f"decode dominant key d={d}")
 
 
 # ------------------------------------------------------------ backward pass
