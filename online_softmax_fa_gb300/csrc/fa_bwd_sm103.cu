@@ -14,23 +14,23 @@
 //           into rows padded to a multiple of 128 per head (the workspace)
 //           so that the dkdv producer fetches a block's rows with bulk copies.
 //   * dkdv: one CTA per (b, h, 128-key block j), query blocks i as the inner
-//           loop.  On tcgen05 with TMEM accumulators: S^T = K_j Q_i^T and
-//           dP^T = V_j dO_i^T (keys are the MMA rows), then eight elementwise
-//           warps (thread = key row = TMEM lane, two warps per row, 64
-//           columns each) form P^T and dS^T in bf16 over the S^T / dP^T
-//           columns, then dV_j += P^T dO_i and
-//           dK_j += dS^T Q_i read them from TMEM.
+//           loop, each taken in two 64-query halves.  On tcgen05 with TMEM
+//           accumulators: S^T = K_j Q_h^T and dP^T = V_j dO_h^T (keys are
+//           the MMA rows) for one half while eight elementwise warps
+//           (thread = key row = TMEM lane, two warps per row, 32 columns
+//           each) form P^T and dS^T in bf16 for the previous half, then
+//           dV_j += P^T dO_h and dK_j += dS^T Q_h read them from TMEM.
 //   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
 //           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
 //           then dQ_i += dS K_j; S is double-buffered, so the next block's S
 //           and dP run on the tensor pipe while the warps work on this one.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
-// is masked.  TMEM (dkdv): S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d, 256+2d); P^T and dS^T are bf16 pairs in the S^T region, over
-// columns [0,32) / [64,96) and [32,64) / [96,128) (each column-half warp
-// writes over its own 64 columns), so dP^T of the next block can be computed
-// while they wait for dV / dK.  TMEM (dq): S [0,128) and [128,256), dP [256,384),
-// dQ [384,384+d).
+// is masked.  Causal CTAs run in cost order across all heads (heaviest
+// first).  TMEM (dkdv): S^T of the two halves at [0,64) and [64,128), dP^T
+// at [128,192) and [192,256), dV [256,256+d), dK [256+d, 256+2d); P^T and
+// dS^T of a half are bf16 pairs over its S^T columns, each column-half warp
+// writing over its own 32 columns (P^T over the first 16, dS^T over the
+// next 16).  TMEM (dq): S [0,128) and [128,256), dP [256,384), dQ [384,384+d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -81,13 +81,14 @@ struct Cfg {
     static constexpr int kOffVq = kOffRing + kStagesK * kTile;      // dq: V ring
     static constexpr int kOffBar = kOffRing + (kRingDkdv > kRingDq ? kRingDkdv : kRingDq);
     // once, full/empty[3] (dkdv: stages; dq: K ring), vfull/vempty[2] (dq: V
-    // ring), s_full[2], p_full, o_full, dp_free
-    static constexpr int kNumBars = 1 + 2 * 3 + 2 * 2 + 5;
+    // ring), s_full[2], p_full[2], o_full, dp_free
+    static constexpr int kNumBars = 1 + 2 * 3 + 2 * 2 + 6;
     static_assert(kStages <= 3 && kStagesK <= 3 && kStagesV <= 2, "barrier slots");
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static constexpr uint32_t kTmS = 0, kTmP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kBlk, kBlk, false);
+    static constexpr uint32_t kIdescHalf = idesc_bf16_f32(kBlk, kBlk / 2, false);
     static constexpr uint32_t kIdescAcc = idesc_bf16_f32(kBlk, D, true);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -137,7 +138,7 @@ __device__ __forceinline__ View<D> view() {
     v.vempty = v.vfull + 2;
     v.s_full = v.vempty + 2;
     v.p_full = v.s_full + 2;
-    v.o_full = v.p_full + 1;
+    v.o_full = v.p_full + 2;
     v.dp_free = v.o_full + 1;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
@@ -168,6 +169,32 @@ __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tm, uint32_t a_tm, uint
                      (acc || kk > 0) ? 1u : 0u);
 }
 
+// M128 x N64 x K(D) for one 64-query half of a block: A = K_j or V_j,
+// B = the half's 64 rows of Q_i or dO_i (both K-major; the caller adds the
+// half's row offset, 64 rows = 8192 bytes = whole swizzle atoms, to B).
+template <int D>
+__device__ __forceinline__ void mma_rows_half(uint32_t d_tm, uint64_t da, uint64_t db) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+        mma_ss_elect(d_tm, da + off, db + off, Cfg<D>::kIdescHalf, kk > 0 ? 1u : 0u);
+    }
+}
+
+// acc[M128 x N(D)] (+)= A[tmem, 128 x 64 bf16] * B[64 rows x D, MN-major]
+// for one 64-query half.  A's bf16 pairs sit in two column groups (each
+// written by one column-half warp over its own 32 fp32 columns): K-steps 0-1
+// at [a, a + 16), 2-3 at [a + 32, a + 48).
+template <int D>
+__device__ __forceinline__ void mma_tmem_half(uint32_t d_tm, uint32_t a_tm, uint64_t db,
+                                              bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < kBlk / 32; ++kk)
+        mma_ts_elect(d_tm, a_tm + (kk >> 1) * 32 + (kk & 1) * 8,
+                     db + static_cast<uint64_t>((kk * 16 * 128) >> 4), Cfg<D>::kIdescAcc,
+                     (acc || kk > 0) ? 1u : 0u);
+}
+
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, uint64_t *bar,
                                           int row, int bh, uint64_t pol) {
@@ -192,7 +219,8 @@ __device__ __forceinline__ void setup_barriers(uint64_t *once, uint64_t *full, u
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kEwWarps);
+    mbar_init(&p_full[0], kEwWarps);
+    mbar_init(&p_full[1], kEwWarps);
     mbar_init(o_full, 1);
     mbar_init(dp_free, kEwWarps);
     *abort_flag = 0;
@@ -239,6 +267,33 @@ __device__ __forceinline__ void p_ds_fast(const uint32_t (&s)[32], const uint32_
     }
 }
 
+// Fast path with the 32 columns' statistics already in registers.
+__device__ __forceinline__ void p_ds_fast_reg(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                              const float4 (&l4)[8], const float4 (&d4)[8],
+                                              float cs, uint32_t (&pp)[16], uint32_t (&pds)[16]) {
+    const uint64_t cs2 = f2_pack(cs, cs);
+#pragma unroll
+    for (int t4 = 0; t4 < 8; ++t4) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = 2 * t4 + h, e = 2 * t;
+            const uint64_t nl = h ? f2_pack(l4[t4].z, l4[t4].w) : f2_pack(l4[t4].x, l4[t4].y);
+            const uint64_t nm = h ? f2_pack(d4[t4].z, d4[t4].w) : f2_pack(d4[t4].x, d4[t4].y);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), cs2, nl),
+                      x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const uint64_t p2 = f2_pack(p0, p1);
+            float ds0, ds1;
+            f2_unpack(f2_mul(p2, f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                        nm)),
+                      ds0, ds1);
+            pp[t] = pack_bf16x2(p0, p1);
+            pds[t] = pack_bf16x2(ds0, ds1);
+        }
+    }
+}
+
 // Masked path (diagonal or ragged block): column col0 + e is kept iff
 // lim_lo <= col0 + e < lim_hi; p = 0 elsewhere.
 __device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint32_t (&dp)[32],
@@ -264,17 +319,21 @@ __device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint3
     }
 }
 
-// Non-blocking test of a barrier phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_ready(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
+// CTA -> (batch x head row, block).  Causal: CTAs in cost order across all
+// heads, heaviest first (key block jb is used by n_blocks - jb query
+// blocks, query block ib by ib + 1 key blocks), so the longest CTAs start in
+// the first wave rather than the last; otherwise head-major.
+template <bool CAUSAL, bool KEY_BLOCKS>
+__device__ __forceinline__ void block_of(const Params &p, int &bh, int &blk) {
+    const int x = static_cast<int>(blockIdx.x);
+    if (CAUSAL) {
+        const int rank = x / p.BH;
+        bh = x - rank * p.BH;
+        blk = KEY_BLOCKS ? rank : p.n_blocks - 1 - rank;
+    } else {
+        bh = x / p.n_blocks;
+        blk = x - bh * p.n_blocks;
+    }
 }
 
 // ============================== dK / dV kernel ==============================
@@ -284,8 +343,8 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
                                             const Params &p, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int jb = blockIdx.x % p.n_blocks;  // key block
+    int bh, jb;  // jb: key block
+    block_of<CAUSAL, true>(p, bh, jb);
     const int N = p.N;
     const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
     const int n_q = p.n_blocks - i0;
@@ -326,18 +385,23 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
     __syncwarp();
 }
 
+// Each 128-query block i is taken in two 64-query halves u = 2t + h, and
+// the halves alternate between two TMEM buffers (buffer h): S^T at
+// [64h, 64h + 64), dP^T at [128 + 64h, 192 + 64h).  The tensor pipe computes
+// S^T and dP^T of half u + 1 while the elementwise warps turn half u into
+// P^T and dS^T, then runs dV / dK of half u, so neither side waits for the
+// other's whole block.
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void dkdv_mma(const Params &p) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int jb = blockIdx.x % p.n_blocks;  // key block
-    const int N = p.N;
-    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
-    const int n_q = p.n_blocks - i0;
+    int bh, jb;  // jb: key block
+    block_of<CAUSAL, true>(p, bh, jb);
+    const int i0 = CAUSAL ? jb : 0;  // first query block touching this key block
+    const int n_u = 2 * (p.n_blocks - i0);  // 64-query halves
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
-    (void)N, (void)tmem, (void)bh;
+    (void)bh;
     // ---- MMA issuer (converged warp, elected lane)
     const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
@@ -346,54 +410,43 @@ __device__ __forceinline__ void dkdv_mma(const Params &p) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
-    const auto so_of = [](int t) {
-        return static_cast<uint64_t>(((t % C::kStages) * 2 * C::kTile) >> 4);
+    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);          // dO after Q
+    const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);         // 64 rows
+    // stage of half u's block, plus the half's row offset
+    const auto so_of = [&](int u) {
+        return static_cast<uint64_t>((((u >> 1) % C::kStages) * 2 * C::kTile) >> 4) +
+               (u & 1) * ho;
     };
-    // P^T and dS^T both land in the S^T region, so the dP^T region is free
-    // as soon as the elementwise warps have read it (dp_free): dP^T of the
-    // next block is issued then when its dO has already arrived (tested
-    // without blocking), else after dV / dK.  S^T of the next block follows
-    // dV / dK (which read P^T and dS^T from its region).
-    bool ok = wait(v.once, 0, kSiteKV);
-    if (ok) ok = wait(&v.full[0], 0, kSiteQ);
-    if (ok) {
+    // S^T(u) = K Q_h^T and dP^T(u) = V dO_h^T into buffer u & 1; a new block
+    // first waits for its stage.
+    const auto issue_sdp = [&](int u) -> bool {
+        const int t = u >> 1;
+        if ((u & 1) == 0 && !wait(&v.full[t % C::kStages], (t / C::kStages) & 1, kSiteQ))
+            return false;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k);       // S^T(0) = K Q_0^T
-        mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + to);  // dP^T(0) = V dO_0^T
-        mma_commit_elect(v.s_full);
-    }
-    for (int t = 0; t < n_q && ok; ++t) {
-        const int t1 = t + 1;
-        const bool more = t1 < n_q;
-        bool early = false;
-        if (more) {
-            ok = wait(v.dp_free, t & 1, kSiteP);
+        const uint64_t so = so_of(u);
+        mma_rows_half<D>(tmem + C::kTmS + (u & 1) * 64, dK, ring_k + so);
+        mma_rows_half<D>(tmem + C::kTmP + (u & 1) * 64, dV, ring_k + so + to);
+        mma_commit_elect(&v.s_full[u & 1]);
+        return true;
+    };
+    bool ok = wait(v.once, 0, kSiteKV);
+    if (ok) ok = issue_sdp(0);
+    for (int u = 0; u < n_u && ok; ++u) {
+        // S^T / dP^T of the next half go into the other buffer, whose P^T /
+        // dS^T were read by dV / dK(u - 1), issued before (in-order pipe)
+        if (u + 1 < n_u) {
+            ok = issue_sdp(u + 1);
             if (!ok) break;
-            early = __all_sync(0xffffffffu,
-                               mbar_ready(&v.full[t1 % C::kStages], (t1 / C::kStages) & 1));
-            if (early) {
-                tc_fence_after();
-                mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so_of(t1) + to);  // dP^T(t+1)
-            }
         }
-        ok = wait(v.p_full, t & 1, kSiteP);
+        ok = wait(&v.p_full[u & 1], (u >> 1) & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t so = so_of(t);
-        mma_tmem_rows<D>(tmem + C::kTmAcc0, tmem + C::kTmS, ring_mn + so + to, t > 0, 0);  // dV
-        mma_tmem_rows<D>(tmem + C::kTmAcc1, tmem + C::kTmS, ring_mn + so, t > 0, 32);      // dK
-        mma_commit_elect(&v.empty[t % C::kStages]);
-        if (more) {
-            if (!early) {
-                ok = wait(&v.full[t1 % C::kStages], (t1 / C::kStages) & 1, kSiteQ);
-                if (!ok) break;
-                tc_fence_after();
-                mma_rows_rows<D>(tmem + C::kTmP, dV, ring_k + so_of(t1) + to);  // dP^T(t+1)
-            }
-            mma_rows_rows<D>(tmem + C::kTmS, dK, ring_k + so_of(t1));  // S^T(t+1)
-            mma_commit_elect(v.s_full);
-        }
+        const uint64_t so = so_of(u);
+        const uint32_t a = tmem + C::kTmS + (u & 1) * 64;
+        mma_tmem_half<D>(tmem + C::kTmAcc0, a, ring_mn + so + to, u > 0);    // dV += P^T dO_h
+        mma_tmem_half<D>(tmem + C::kTmAcc1, a + 16, ring_mn + so, u > 0);    // dK += dS^T Q_h
+        if (u & 1) mma_commit_elect(&v.empty[(u >> 1) % C::kStages]);      // block's stage read
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
@@ -403,92 +456,86 @@ template <int D, bool CAUSAL>
 __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int jb = blockIdx.x % p.n_blocks;  // key block
+    int bh, jb;  // jb: key block
+    block_of<CAUSAL, true>(p, bh, jb);
     const int N = p.N;
-    const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
-    const int n_q = p.n_blocks - i0;
+    const int i0 = CAUSAL ? jb : 0;  // first query block touching this key block
+    const int n_u = 2 * (p.n_blocks - i0);
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
-    (void)N, (void)tmem, (void)bh;
-    // ---- elementwise: thread = key row of this block (TMEM lane), warp
-    // half h = columns (queries) [64h, 64h + 64)
-    const int quarter = warp & 3, half = warp >> 2;
+    // ---- elementwise: thread = key row of this block (TMEM lane); warp
+    // column half c = queries [32c, 32c + 32) of each 64-query half
+    const int quarter = warp & 3, c = warp >> 2;
     const int row = quarter * 32 + lane;
     const int key = jb * kBlk + row;
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
-    const int cb = half * 64;
     bool ok = true;
-    for (int t = 0; t < n_q && ok; ++t) {
-        const int s = t % C::kStages;
-        ok = mbar_wait(v.s_full, t & 1, ctl, kSiteS);
+    for (int u = 0; u < n_u && ok; ++u) {
+        const int t = u >> 1, h = u & 1, s = t % C::kStages;
         // the stage's LSE2/D rows landed with its tiles (the stage cannot
-        // be refilled before this block's p_full)
-        if (ok) ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
+        // be refilled before this block's last dV / dK); this warp's 32
+        // columns of them go to registers before S^T / dP^T are waited for
+        ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
+        if (!ok) break;
+        const int q0 = (i0 + t) * kBlk;
+        const int cb = 64 * h + 32 * c;  // this warp's first column within the block
+        const float *lse2 = v.rows + s * 2 * kBlk + cb, *dd = lse2 + kBlk;
+        float4 l4[8], d4[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            l4[e] = reinterpret_cast<const float4 *>(lse2)[e];
+            d4[e] = reinterpret_cast<const float4 *>(dd)[e];
+        }
+        ok = mbar_wait(&v.s_full[h], (u >> 1) & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
-        const int q0 = (i0 + t) * kBlk;
-        const float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
         // column (query) q kept iff q < N and, causal, q >= key
         const int lim_lo = CAUSAL ? key - q0 : 0;
         const int lim_hi = N - q0;
-        // this warp's 64 columns of S^T and dP^T in one round trip; P^T
-        // and dS^T (bf16 pairs) go over the first 32 of those columns
-        uint32_t s0[32], s1[32], d0[32], d1[32], pp[16], pds[16];
-        const uint32_t ts = tmem + lb + C::kTmS + cb, tp = tmem + lb + C::kTmP + cb;
-        tmem_ld32x4(ts, ts + 32, tp, tp + 32, s0, s1, d0, d1);
-        // dP^T is in registers: the MMA warp may compute the next one over it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(v.dp_free);
+        uint32_t sv[32], dv[32], pp[16], pds[16];
+        const uint32_t ts = tmem + lb + C::kTmS + 64 * h + 32 * c;
+        const uint32_t tp = tmem + lb + C::kTmP + 64 * h + 32 * c;
+        tmem_ld32x2(ts, tp, sv, dv);
         // masked only on the diagonal block (causal) and a ragged last block
         const bool masked = (CAUSAL && t == 0) || q0 + kBlk > N;
         if (masked)
-            p_ds_masked(s0, d0, lse2 + cb, dd + cb, true, 0.f, 0.f, p.scale_log2, lim_lo,
-                        lim_hi, cb, pp, pds);
+            p_ds_masked(sv, dv, lse2, dd, true, 0.f, 0.f, p.scale_log2, lim_lo, lim_hi, cb, pp,
+                        pds);
         else
-            p_ds_fast(s0, d0, lse2 + cb, dd + cb, true, 0.f, 0.f, p.scale_log2, pp, pds);
-        // P^T over the first 32 columns of this warp's S^T slice, dS^T over
-        // the next 32
+            p_ds_fast_reg(sv, dv, l4, d4, p.scale_log2, pp, pds);
+        // P^T over the first 16 of this warp's 32 S^T columns, dS^T over the
+        // next 16
         tmem_st16(ts, pp);
-        tmem_st16(ts + 32, pds);
-        if (masked)
-            p_ds_masked(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2,
-                        lim_lo, lim_hi, cb + 32, pp, pds);
-        else
-            p_ds_fast(s1, d1, lse2 + cb + 32, dd + cb + 32, true, 0.f, 0.f, p.scale_log2, pp,
-                      pds);
-        tmem_st16(ts + 16, pp);
-        tmem_st16(ts + 48, pds);
+        tmem_st16(ts + 16, pds);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(v.p_full);
+        if (lane == 0) mbar_arrive(&v.p_full[h]);
     }
     if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
     if (ok) {
         tc_fence_after();
         const bool in = key < N;
-        __nv_bfloat16 *dv = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
-        __nv_bfloat16 *dk = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
+        __nv_bfloat16 *dvp = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
+        __nv_bfloat16 *dkp = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
 #pragma unroll 1
-        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {  // half the columns
+        for (int g = c * (D / 64); g < (c + 1) * (D / 64); ++g) {  // half the columns
             uint32_t a[32], b[32], pa[16], pb[16];
-            tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * c, a);
-            tmem_ld32(tmem + lb + C::kTmAcc1 + 32 * c, b);
+            tmem_ld32(tmem + lb + C::kTmAcc0 + 32 * g, a);
+            tmem_ld32(tmem + lb + C::kTmAcc1 + 32 * g, b);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
-                pb[t] = pack_bf16x2(__uint_as_float(b[2 * t]) * p.scale,
-                                    __uint_as_float(b[2 * t + 1]) * p.scale);
+            for (int e = 0; e < 16; ++e) {
+                pa[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                pb[e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale,
+                                    __uint_as_float(b[2 * e + 1]) * p.scale);
             }
             if (in) {
-                uint4 *o0 = reinterpret_cast<uint4 *>(dv + 32 * c);
-                uint4 *o1 = reinterpret_cast<uint4 *>(dk + 32 * c);
+                uint4 *o0 = reinterpret_cast<uint4 *>(dvp + 32 * g);
+                uint4 *o1 = reinterpret_cast<uint4 *>(dkp + 32 * g);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    o0[t] = make_uint4(pa[4 * t], pa[4 * t + 1], pa[4 * t + 2], pa[4 * t + 3]);
-                    o1[t] = make_uint4(pb[4 * t], pb[4 * t + 1], pb[4 * t + 2], pb[4 * t + 3]);
+                for (int e = 0; e < 4; ++e) {
+                    o0[e] = make_uint4(pa[4 * e], pa[4 * e + 1], pa[4 * e + 2], pa[4 * e + 3]);
+                    o1[e] = make_uint4(pb[4 * e], pb[4 * e + 1], pb[4 * e + 2], pb[4 * e + 3]);
                 }
             }
         }
@@ -542,9 +589,8 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
                                             const Params &p, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
-                          : blockIdx.x % p.n_blocks;
+    int bh, ib;  // ib: query block
+    block_of<CAUSAL, false>(p, bh, ib);
     const int N = p.N;
     const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
     const uint32_t tmem = *v.tmem_slot;
@@ -585,9 +631,8 @@ template <int D, bool CAUSAL>
 __device__ __forceinline__ void dq_mma(const Params &p) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
-                          : blockIdx.x % p.n_blocks;
+    int bh, ib;  // ib: query block
+    block_of<CAUSAL, false>(p, bh, ib);
     const int N = p.N;
     const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
     const uint32_t tmem = *v.tmem_slot;
@@ -654,9 +699,8 @@ template <int D, bool CAUSAL>
 __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    const int bh = blockIdx.x / p.n_blocks;
-    const int ib = CAUSAL ? (p.n_blocks - 1 - blockIdx.x % p.n_blocks)  // heavy first
-                          : blockIdx.x % p.n_blocks;
+    int bh, ib;  // ib: query block
+    block_of<CAUSAL, false>(p, bh, ib);
     const int N = p.N;
     const int n_k = CAUSAL ? ib + 1 : p.n_blocks;  // key blocks at or below the diagonal
     const uint32_t tmem = *v.tmem_slot;

@@ -320,6 +320,23 @@ __device__ __forceinline__ void tmem_ld128_max(uint32_t taddr, uint32_t (&r)[128
         : "memory");
 }
 
+// Two 32-column loads from this warp's lane quarter, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t (&r)[32],
+                                            uint32_t (&q)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : FA_R8X(r, 0), FA_R8X(r, 8), FA_R8X(r, 16), FA_R8X(r, 24), FA_R8X(q, 0), FA_R8X(q, 8),
+          FA_R8X(q, 16), FA_R8X(q, 24)
+        : "r"(a0), "r"(a1)
+        : "memory");
+}
+
 // Four x32 loads (any four 32-column groups of this warp's lanes), one wait.
 __device__ __forceinline__ void tmem_ld32x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                             uint32_t (&r)[32], uint32_t (&q)[32],
