@@ -25,8 +25,8 @@
 //           then dQ_i += dS K_j; S is double-buffered, so the next block's S
 //           and dP run on the tensor pipe while the warps work on this one.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
-// is masked.  Causal CTAs run in cost order across all heads (heaviest
-// first).  TMEM (dkdv): S^T of the two halves at [0,64) and [64,128), dP^T
+// is masked.  Causal CTAs run in cost order (heaviest first) within groups
+// of heads small enough to share L2.  TMEM (dkdv): S^T of the two halves at [0,64) and [64,128), dP^T
 // at [128,192) and [192,256), dV [256,256+d), dK [256+d, 256+2d); P^T and
 // dS^T of a half are bf16 pairs over its S^T columns, each column-half warp
 // writing over its own 32 columns (P^T over the first 16, dS^T over the
@@ -104,6 +104,7 @@ struct Params {
     const float *lse2;  // -LSE * log2(e)
     const float *dd;    // -D, D = rowsum(dO * O)
     int N, BH, n_blocks;
+    int head_group;  // causal CTA order: heads per group (see block_of)
     float scale, scale_log2;
     uint64_t limit_ns;
 };
@@ -319,16 +320,24 @@ __device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint3
     }
 }
 
-// CTA -> (batch x head row, block).  Causal: CTAs in cost order across all
-// heads, heaviest first (key block jb is used by n_blocks - jb query
-// blocks, query block ib by ib + 1 key blocks), so the longest CTAs start in
-// the first wave rather than the last; otherwise head-major.
+// CTA -> (batch x head row, block).  Causal: the heads are taken in groups
+// of head_group, and within a group the CTAs run in cost order, heaviest
+// first (key block jb is used by n_blocks - jb query blocks, query block ib
+// by ib + 1 key blocks), so the longest CTAs start early instead of in the
+// last wave, while the CTAs in flight share a group's K/V/Q/dO in L2 (the
+// host sizes the group so that its heaviest CTAs still start early enough).
+// Otherwise head-major.
 template <bool CAUSAL, bool KEY_BLOCKS>
 __device__ __forceinline__ void block_of(const Params &p, int &bh, int &blk) {
     const int x = static_cast<int>(blockIdx.x);
     if (CAUSAL) {
-        const int rank = x / p.BH;
-        bh = x - rank * p.BH;
+        const int per_group = p.head_group * p.n_blocks;
+        const int grp = x / per_group;
+        const int in = x - grp * per_group;
+        const int h0 = grp * p.head_group;
+        const int gsize = min(p.head_group, p.BH - h0);  // the last group may be smaller
+        const int rank = in / gsize;
+        bh = h0 + (in - rank * gsize);
         blk = KEY_BLOCKS ? rank : p.n_blocks - 1 - rank;
     } else {
         bh = x / p.n_blocks;
@@ -890,6 +899,16 @@ static int launch_bwd_t(const BwdArgs &a) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * bwd::kLog2e;
     p.limit_ns = a.limit_ns;
+    // Causal CTA order: a group of heads holds enough work that its heaviest
+    // CTAs (about 2 / (n_blocks + 1) of a head's work each) start well
+    // before the end even when the group runs last: about 3 x SMs / (n_blocks
+    // + 1) heads.
+    int sms = 0;
+    FA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    {
+        const long long g = (3LL * (sms > 0 ? sms : 1) + n_blocks) / (n_blocks + 1);
+        p.head_group = static_cast<int>(g < 1 ? 1 : (g > a.BH ? a.BH : g));
+    }
     const long long grid = static_cast<long long>(p.n_blocks) * a.BH;
     if (grid > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
     p.g0 = static_cast<__nv_bfloat16 *>(a.dK);
