@@ -189,10 +189,10 @@ namespace {
 // kept for the life of the process; `mu` serialises the enqueueing of calls
 // that share them.
 struct HostPipe {
-    static constexpr int kMaxChunks = 8;
+    static constexpr int kMaxChunks = 16;
     std::mutex mu;
     bool ready = false;
-    cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+    cudaStream_t in = nullptr, comp[2] = {nullptr, nullptr}, out = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
 };
@@ -203,7 +203,8 @@ int host_pipe_init(HostPipe &h) {
     if (h.ready) return FA_OK;
     const unsigned fl = cudaStreamNonBlocking;
     FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.in, fl));
-    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.comp, fl));
+    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.comp[0], fl));
+    FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.comp[1], fl));
     FA_CUDA_TRY(cudaStreamCreateWithFlags(&h.out, fl));
     FA_CUDA_TRY(cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming));
     FA_CUDA_TRY(cudaEventCreateWithFlags(&h.done, cudaEventDisableTiming));
@@ -213,6 +214,45 @@ int host_pipe_init(HostPipe &h) {
     }
     h.ready = true;
     return FA_OK;
+}
+
+// Chunk boundaries (in heads) for the host-buffer pipeline: chunks of
+// `size` heads, except that the last chunks shrink by halves down to one
+// head (..., 4, 2, 1, 1), so that little work waits for the last copy-in
+// and little output for the last kernel.  Falls back to equal chunks when
+// that would take more than kMaxChunks.  Returns the chunk count; chunk c
+// covers heads [bounds[c], bounds[c + 1]).
+int plan_chunks(long long BH, long long equal_chunks, long long *bounds) {
+    const long long size = (BH + equal_chunks - 1) / equal_chunks;
+    long long tail[HostPipe::kMaxChunks];
+    int nt = 0;
+    long long used = 0;
+    for (long long sz = 1; sz < size && used + sz <= BH && nt < HostPipe::kMaxChunks; sz *= 2) {
+        tail[nt++] = sz;
+        used += sz;
+        if (sz == 1 && used + 1 <= BH && nt < HostPipe::kMaxChunks) {  // two chunks of one head
+            tail[nt++] = 1;
+            used += 1;
+        }
+    }
+    const long long full = (BH - used + size - 1) / size;
+    if (size <= 1 || full + nt > HostPipe::kMaxChunks) {  // equal chunks
+        for (long long c = 0; c <= equal_chunks; ++c) bounds[c] = c * BH / equal_chunks;
+        return static_cast<int>(equal_chunks);
+    }
+    int n = 0;
+    bounds[0] = 0;
+    // the first chunk takes the remainder, the others `size` heads each
+    long long h = BH - used - (full - 1) * size;
+    for (long long c = 0; c < full; ++c) {
+        bounds[n + 1] = bounds[n] + (c == 0 ? h : size);
+        ++n;
+    }
+    for (int i = nt - 1; i >= 0; --i) {
+        bounds[n + 1] = bounds[n] + tail[i];
+        ++n;
+    }
+    return n;
 }
 }  // namespace
 
@@ -237,10 +277,13 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
 
     // The heads are independent, so the work is cut into chunks of heads:
     // the copy-in of chunk c+1, the kernel on chunk c and the copy-out of
-    // chunk c-1 overlap on three streams.  Each chunk keeps at least about
-    // one query block per SM, so the kernel stays reasonably efficient while
-    // the copies (the longer part) hide it; the results are those of one
-    // fa_fwd call (each head is computed the same way).
+    // chunk c-1 overlap (one copy-in stream, two kernel streams taken in
+    // turn, one copy-out stream).  Most chunks keep at least about one query
+    // block per SM, so the kernel stays reasonably efficient while the
+    // copies (the longer part) hide it; the last chunks shrink (plan_chunks)
+    // and their kernels overlap each other on the two kernel streams.  The
+    // results are those of one fa_fwd call (each head is computed the same
+    // way).
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
     int sms = 0;
@@ -248,10 +291,12 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
     const long long BH = static_cast<long long>(B) * H;
     const long long rows_per_item = d == 256 ? 128 : 256;
     const long long qblocks = (static_cast<long long>(N) + rows_per_item - 1) / rows_per_item;
-    long long chunks = BH * qblocks / (sms > 0 ? sms : 1);
-    if (chunks > HostPipe::kMaxChunks) chunks = HostPipe::kMaxChunks;
-    if (chunks > BH) chunks = BH;
-    if (chunks < 1) chunks = 1;
+    long long equal = BH * qblocks / (sms > 0 ? sms : 1);
+    if (equal > 8) equal = 8;
+    if (equal > BH) equal = BH;
+    if (equal < 1) equal = 1;
+    long long bounds[HostPipe::kMaxChunks + 1];
+    const int chunks = plan_chunks(BH, equal, bounds);
     if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
     HostPipe *hp = &g_pipes[dev];
     std::lock_guard<std::mutex> lock(hp->mu);
@@ -260,11 +305,13 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
     // everything below runs after the caller's earlier work on `stream`
     FA_CUDA_TRY(cudaEventRecord(hp->start, s));
     FA_CUDA_TRY(cudaStreamWaitEvent(hp->in, hp->start, 0));
-    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp, hp->start, 0));
+    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp[0], hp->start, 0));
+    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp[1], hp->start, 0));
     FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->start, 0));
     const size_t head_t = static_cast<size_t>(N) * d * 2, head_l = static_cast<size_t>(N) * 4;
-    for (long long c = 0; c < chunks; ++c) {
-        const long long h0 = c * BH / chunks, h1 = (c + 1) * BH / chunks;
+    for (int c = 0; c < chunks; ++c) {
+        const long long h0 = bounds[c], h1 = bounds[c + 1];
+        cudaStream_t comp = hp->comp[c & 1];
         const size_t off_t = h0 * head_t, n_t = (h1 - h0) * head_t;
         const size_t off_l = h0 * head_l, n_l = (h1 - h0) * head_l;
         FA_CUDA_TRY(cudaMemcpyAsync(dQ + off_t, static_cast<const uint8_t *>(Q_host) + off_t, n_t,
@@ -274,14 +321,14 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
         FA_CUDA_TRY(cudaMemcpyAsync(dV + off_t, static_cast<const uint8_t *>(V_host) + off_t, n_t,
                                     cudaMemcpyHostToDevice, hp->in));
         FA_CUDA_TRY(cudaEventRecord(hp->loaded[c], hp->in));
-        FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp, hp->loaded[c], 0));
+        FA_CUDA_TRY(cudaStreamWaitEvent(comp, hp->loaded[c], 0));
         // one batch of h1 - h0 heads (B = 1): MHA heads need no batch index
         rc = fa_fwd(dQ + off_t, dK + off_t, dV + off_t, dO + off_t,
                     reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dL) + off_l), 1,
                     static_cast<int>(h1 - h0), N, d, causal, scale,
-                    reinterpret_cast<fa_stream_t>(hp->comp));
+                    reinterpret_cast<fa_stream_t>(comp));
         if (rc != FA_OK) return rc;
-        FA_CUDA_TRY(cudaEventRecord(hp->computed[c], hp->comp));
+        FA_CUDA_TRY(cudaEventRecord(hp->computed[c], comp));
         FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->computed[c], 0));
         FA_CUDA_TRY(cudaMemcpyAsync(static_cast<uint8_t *>(O_host) + off_t, dO + off_t, n_t,
                                     cudaMemcpyDeviceToHost, hp->out));
@@ -290,8 +337,8 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
                                     cudaMemcpyDeviceToHost, hp->out));
     }
     // the caller's stream resumes once the last copy-out is done (the
-    // copy-out stream has waited for every kernel, which waited for every
-    // copy-in)
+    // copy-out stream has waited for every kernel, in order, and each
+    // kernel for its copy-in)
     FA_CUDA_TRY(cudaEventRecord(hp->done, hp->out));
     FA_CUDA_TRY(cudaStreamWaitEvent(s, hp->done, 0));
     return FA_OK;
