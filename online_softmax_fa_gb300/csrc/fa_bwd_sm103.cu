@@ -20,6 +20,7 @@
 //           (thread = key row = TMEM lane, two warps per row, 32 columns
 //           each) form P^T and dS^T in bf16 for the previous half, then
 //           dV_j += P^T dO_h and dK_j += dS^T Q_h read them from TMEM.
+//           Two warps issue the MMAs: one S^T / dP^T, one dV / dK.
 //   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
 //           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
 //           then dQ_i += dS K_j; S is double-buffered, so the next block's S
@@ -51,12 +52,12 @@ namespace bwd {
 constexpr int kBlk = 128;             // rows per block (keys or queries)
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 constexpr int kEwWarps = 8;           // elementwise warps: 4 lane quarters x 2 column halves
-constexpr int kThreads = 384;         // 3 warpgroups: 8 elementwise warps, MMA, TMA, 2 idle
+constexpr int kThreads = 384;         // 3 warpgroups: 8 elementwise warps, MMA (warp 8; dkdv also 10), TMA (9)
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-// Registers after reallocation: 128 x (216 + 216 + 64) = 63488 <= 384 x 168.
+// Registers after reallocation: 128 x (216 + 216 + 72) = 64512 = 384 x 168.
 constexpr uint32_t kRegsEw = 216;
-constexpr uint32_t kRegsCtl = 64;
+constexpr uint32_t kRegsCtl = 72;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -400,62 +401,87 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
 // S^T and dP^T of half u + 1 while the elementwise warps turn half u into
 // P^T and dS^T, then runs dV / dK of half u, so neither side waits for the
 // other's whole block.
+// Two issuing warps: warp 8 issues S^T / dP^T of each half, warp 10 the dV
+// / dK of each half once its P^T / dS^T are in TMEM.  S^T / dP^T(u) go into
+// buffer u & 1 after dV / dK(u - 2), which read that buffer, have completed
+// (buf_free, committed by warp 10; the dkdv kernel uses the dq kernel's V
+// ring barriers vfull[2] for it).  Warp 10's commit after the second half's
+// dV / dK releases the block's stage: that dV / dK followed the half's
+// p_full, so the S^T / dP^T that read the stage had completed too.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void dkdv_mma(const Params &p) {
+__device__ __forceinline__ void dkdv_issue_sdp(const Params &p) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
     int bh, jb;  // jb: key block
     block_of<CAUSAL, true>(p, bh, jb);
-    const int i0 = CAUSAL ? jb : 0;  // first query block touching this key block
+    const int i0 = CAUSAL ? jb : 0;
     const int n_u = 2 * (p.n_blocks - i0);  // 64-query halves
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     (void)bh;
-    // ---- MMA issuer (converged warp, elected lane)
     const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
     const uint64_t ring_k = sdesc_sw128(smem_u32(v.ring), 16, 1024);
+    const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+    };
+    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+    const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);
+    uint64_t *buf_free = v.vfull;
+    bool ok = wait(v.once, 0, kSiteKV);
+    for (int u = 0; u < n_u && ok; ++u) {
+        const int t = u >> 1;
+        if ((u & 1) == 0) {
+            ok = wait(&v.full[t % C::kStages], (t / C::kStages) & 1, kSiteQ);
+            if (!ok) break;
+        }
+        if (u >= 2) {
+            ok = wait(&buf_free[u & 1], ((u - 2) >> 1) & 1, kSiteP);
+            if (!ok) break;
+        }
+        tc_fence_after();
+        const uint64_t so =
+            static_cast<uint64_t>(((t % C::kStages) * 2 * C::kTile) >> 4) + (u & 1) * ho;
+        mma_rows_half<D>(tmem + C::kTmS + (u & 1) * 64, dK, ring_k + so);
+        mma_rows_half<D>(tmem + C::kTmP + (u & 1) * 64, dV, ring_k + so + to);
+        mma_commit_elect(&v.s_full[u & 1]);
+    }
+    // every MMA of this warp had completed before the other issuer's last
+    // dV / dK (it followed the last p_full); wait for that one
+    mbar_wait_drain(v.o_full, 0, p.limit_ns);
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void dkdv_issue_acc(const Params &p) {
+    using C = Cfg<D>;
+    const View<D> v = view<D>();
+    int bh, jb;  // jb: key block
+    block_of<CAUSAL, true>(p, bh, jb);
+    const int i0 = CAUSAL ? jb : 0;
+    const int n_u = 2 * (p.n_blocks - i0);
+    const uint32_t tmem = *v.tmem_slot;
+    const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
+    (void)bh;
     const uint64_t ring_mn = sdesc_sw128(smem_u32(v.ring), kBoxBytes, 1024);
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);          // dO after Q
-    const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);         // 64 rows
-    // stage of half u's block, plus the half's row offset
-    const auto so_of = [&](int u) {
-        return static_cast<uint64_t>((((u >> 1) % C::kStages) * 2 * C::kTile) >> 4) +
-               (u & 1) * ho;
-    };
-    // S^T(u) = K Q_h^T and dP^T(u) = V dO_h^T into buffer u & 1; a new block
-    // first waits for its stage.
-    const auto issue_sdp = [&](int u) -> bool {
-        const int t = u >> 1;
-        if ((u & 1) == 0 && !wait(&v.full[t % C::kStages], (t / C::kStages) & 1, kSiteQ))
-            return false;
-        tc_fence_after();
-        const uint64_t so = so_of(u);
-        mma_rows_half<D>(tmem + C::kTmS + (u & 1) * 64, dK, ring_k + so);
-        mma_rows_half<D>(tmem + C::kTmP + (u & 1) * 64, dV, ring_k + so + to);
-        mma_commit_elect(&v.s_full[u & 1]);
-        return true;
-    };
-    bool ok = wait(v.once, 0, kSiteKV);
-    if (ok) ok = issue_sdp(0);
+    const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
+    const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);
+    uint64_t *buf_free = v.vfull;
+    bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        // S^T / dP^T of the next half go into the other buffer, whose P^T /
-        // dS^T were read by dV / dK(u - 1), issued before (in-order pipe)
-        if (u + 1 < n_u) {
-            ok = issue_sdp(u + 1);
-            if (!ok) break;
-        }
         ok = wait(&v.p_full[u & 1], (u >> 1) & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t so = so_of(u);
+        const int t = u >> 1;
+        const uint64_t so =
+            static_cast<uint64_t>(((t % C::kStages) * 2 * C::kTile) >> 4) + (u & 1) * ho;
         const uint32_t a = tmem + C::kTmS + (u & 1) * 64;
-        mma_tmem_half<D>(tmem + C::kTmAcc0, a, ring_mn + so + to, u > 0);    // dV += P^T dO_h
-        mma_tmem_half<D>(tmem + C::kTmAcc1, a + 16, ring_mn + so, u > 0);    // dK += dS^T Q_h
-        if (u & 1) mma_commit_elect(&v.empty[(u >> 1) % C::kStages]);      // block's stage read
+        mma_tmem_half<D>(tmem + C::kTmAcc0, a, ring_mn + so + to, u > 0);  // dV += P^T dO_h
+        mma_tmem_half<D>(tmem + C::kTmAcc1, a + 16, ring_mn + so, u > 0);  // dK += dS^T Q_h
+        mma_commit_elect(&buf_free[u & 1]);
+        if (u & 1) mma_commit_elect(&v.empty[t % C::kStages]);
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
@@ -573,11 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each role runs inside the branch that set its register budget and
     // rebuilds what it needs, so little stays live across the switch.
     if (warp >= kMmaWarp) {
-        regs_decrease<kRegsCtl>();  // warps 10, 11: no role
+        regs_decrease<kRegsCtl>();  // warp 11: no role
         if (warp == kTmaWarp)
             dkdv_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, &tmdO, p, lane);
         else if (warp == kMmaWarp)
-            dkdv_mma<D, CAUSAL>(p);
+            dkdv_issue_sdp<D, CAUSAL>(p);
+        else if (warp == kMmaWarp + 2)
+            dkdv_issue_acc<D, CAUSAL>(p);
         __syncwarp();
     } else {
         regs_increase<kRegsEw>();
