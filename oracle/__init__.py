@@ -228,6 +228,32 @@ def attention_bwd(q, k, v, do, causal: bool = False, scale: float | None = None,
     return out
 
 
+def attention_bwd_gqa(q, k, v, do, causal: bool = False, scale: float | None = None,
+                      nthreads: int | None = None):
+    """Gradients (dQ, dK, dV) of grouped-query attention ("Understanding
+    FlashAttention Pt 1", section 4.1: query head h uses K/V head
+    h // (H / H_kv)) for the output gradient dO.  q, do [B, H, N, d]; k, v
+    [B, H_kv, N, d].  Grouped-query attention is the dense forward pass on
+    K/V heads repeated for their group, so by the chain rule a K/V head's
+    gradient is the sum of the dense gradients of its repeats; dQ is the
+    dense one.  Returns dQ [B, H, N, d], dK and dV [B, H_kv, N, d]."""
+    q, k, v, do = (_as_f64(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")))
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or do.shape != q.shape:
+        raise ValueError("expected q, do [B,H,N,d] and k, v [B,H_kv,N,d]")
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    if k.shape[0] != B or k.shape[2:] != (N, d) or H_kv < 1 or H % H_kv:
+        raise ValueError("shape mismatch")
+    group = H // H_kv
+    k_full = np.repeat(k, group, axis=1)
+    v_full = np.repeat(v, group, axis=1)
+    dq, dk_full, dv_full = attention_bwd(q, k_full, v_full, do, causal=causal, scale=scale,
+                                         nthreads=nthreads)
+    dk = dk_full.reshape(B, H_kv, group, N, d).sum(axis=2)
+    dv = dv_full.reshape(B, H_kv, group, N, d).sum(axis=2)
+    return dq, dk, dv
+
+
 def attention_fwd_blockwise(q, k, v, bounds, causal: bool = False,
                             scale: float | None = None, reverse: bool = False,
                             rows=None, nthreads: int | None = None,

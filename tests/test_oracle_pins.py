@@ -402,6 +402,36 @@ def test_backward_matches_finite_differences(causal):
         np.testing.assert_allclose(g, num, atol=1e-7, rtol=1e-6)
 
 
+def _loss_gqa(q, k, v, do, causal, scale):
+    O, _ = oracle.attention_fwd_gqa(q, k, v, causal=causal, scale=scale)
+    return float(np.sum(O * do))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_gqa_matches_finite_differences(causal):
+    """Grouped-query gradients by central differences of sum(O * dO) with O
+    from the grouped-query forward oracle: every element of Q and of the
+    shared K and V heads (four query heads on two K/V heads)."""
+    rng = np.random.default_rng(50 + causal)
+    B, H, H_kv, N, d, scale = 1, 4, 2, 5, 3, 0.6
+    q, do = (rng.standard_normal((B, H, N, d)) for _ in range(2))
+    k, v = (rng.standard_normal((B, H_kv, N, d)) for _ in range(2))
+    dq, dk, dv = oracle.attention_bwd_gqa(q, k, v, do, causal=causal, scale=scale)
+    assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            x0 = x[idx]
+            x[idx] = x0 + eps
+            fp = _loss_gqa(q, k, v, do, causal, scale)
+            x[idx] = x0 - eps
+            fm = _loss_gqa(q, k, v, do, causal, scale)
+            x[idx] = x0
+            num[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(g, num, atol=1e-7, rtol=1e-6)
+
+
 def test_backward_identities():
     """Rows of dS sum to zero, so shifting every key by u leaves dQ unchanged
     and every key-gradient sum is zero; D_i = sum_r dO_ir O_ir."""
