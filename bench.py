@@ -452,14 +452,18 @@ def run_backward(args, w, causal):
     q, k, v = make_workload(w)
     do = make_grad(w.B, w.H, w.N, w.d, w.seed)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=w.scale)
-    grads = [tuple(torch.empty_like(qd) for _ in range(3)) for _ in range(2)]
+    gqa = bool(w.H_kv) and w.H_kv != w.H
+    fwd = fa.fa_fwd_gqa if gqa else fa.fa_fwd
+    bwd = fa.fa_bwd_gqa if gqa else fa.fa_bwd
+    o, lse = fwd(qd, kd, vd, causal=causal, scale=w.scale)
+    grads = [(torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
+             for _ in range(2)]
     wsb = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
                       device=dev)
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):
         dq, dk, dv = grads[i % 2]
-        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
+        bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws_)
@@ -467,7 +471,7 @@ def run_backward(args, w, causal):
     e0.record(stream)
     for i in range(args.steps):
         dq, dk, dv = grads[i % 2]
-        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
+        bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, wsb, causal=causal, scale=w.scale)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws_)

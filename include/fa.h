@@ -158,6 +158,32 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
            fa_stream_t stream);
 
 /*
+ * fa_bwd_gqa -- fa_bwd for grouped-query (and multi-query) attention, the
+ * gradients of fa_fwd_gqa: H query heads share H_kv K/V heads, query head h
+ * of a batch reading K/V head h / (H / H_kv) ("Understanding FlashAttention
+ * Pt 1", section 4.1).  The forward pass is the dense one on K/V heads
+ * repeated for their group, so a K/V head's gradient is the sum of the
+ * dense gradients of its repeats; dQ is the dense one.
+ *
+ *   Q, O, dO        bf16 [B, H, N, d], device, read
+ *   K, V            bf16 [B, H_kv, N, d], device, read
+ *   LSE             fp32 [B, H, N], device, read
+ *   dQ              bf16 [B, H, N, d], device, written
+ *   dK, dV          bf16 [B, H_kv, N, d], device, written
+ *   H_kv            >= 1 and dividing H (FA_ERR_SHAPE otherwise)
+ *   workspace       as fa_bwd: fa_bwd_workspace_bytes(B, H, N, d) bytes
+ * The dK/dV kernel runs one CTA per (K/V head, key block) and walks the
+ * query blocks of every query head of the group in turn, so the group sum
+ * is accumulated in TMEM in a fixed order: deterministic, no atomics.
+ * fa_bwd(...) is fa_bwd_gqa with H_kv = H.  Other checks and errors as
+ * fa_bwd.
+ */
+int fa_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+               const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
+               size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int causal,
+               float scale, fa_stream_t stream);
+
+/*
  * fa_decode_workspace_bytes -- device workspace fa_decode needs: the
  * per-split softmax states (m, l and the d-wide accumulator for every
  * query head and key split).  Returns 0 for an invalid or unsupported shape.

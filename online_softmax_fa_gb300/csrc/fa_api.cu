@@ -458,9 +458,18 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
            const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
            size_t workspace_bytes, int B, int H, int N, int d, int causal, float scale,
            fa_stream_t stream) {
+    return fa_bwd_gqa(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, H, N,
+                      d, causal, scale, stream);
+}
+
+int fa_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+               const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
+               size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int causal,
+               float scale, fa_stream_t stream) {
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_NULL;
     int rc = check_shape(B, H, N, d, scale);
     if (rc != FA_OK) return rc;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
     const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
     if (mis16(Q) || mis16(K) || mis16(V) || mis16(O) || mis16(dO) || mis16(dQ) || mis16(dK) ||
         mis16(dV) || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0)
@@ -470,11 +479,12 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FA_ERR_WORKSPACE;
     const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
     const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
     const struct { const void *p; size_t n; } ins[] = {
-        {Q, t_bytes}, {K, t_bytes}, {V, t_bytes}, {O, t_bytes}, {dO, t_bytes}, {LSE, l_bytes}};
+        {Q, t_bytes}, {K, kv_bytes}, {V, kv_bytes}, {O, t_bytes}, {dO, t_bytes}, {LSE, l_bytes}};
     const struct { const void *p; size_t n; } outs[] = {
-        {dQ, t_bytes}, {dK, t_bytes}, {dV, t_bytes}, {workspace, need}};
+        {dQ, t_bytes}, {dK, kv_bytes}, {dV, kv_bytes}, {workspace, need}};
     for (const auto &o : outs) {
         for (const auto &in : ins)
             if (overlaps(o.p, o.n, in.p, in.n)) return FA_ERR_ALIAS;
@@ -485,8 +495,8 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
     if (rc != FA_OK) return rc;
     CUtensorMap tmQ, tmK, tmV, tmdO;
     const int BH = B * H;
-    if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, BH, N, d) ||
-        !encode_qkv_map(&tmV, V, BH, N, d) || !encode_qkv_map(&tmdO, dO, BH, N, d))
+    if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, B * H_kv, N, d) ||
+        !encode_qkv_map(&tmV, V, B * H_kv, N, d) || !encode_qkv_map(&tmdO, dO, BH, N, d))
         return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     fa::BwdArgs a;
     a.tmQ = &tmQ;
@@ -503,6 +513,8 @@ int fa_bwd(const void *Q, const void *K, const void *V, const void *O, const voi
     a.BH = BH;
     a.N = N;
     a.d = d;
+    a.H = H;
+    a.Hkv = H_kv;
     a.causal = causal != 0;
     a.scale = scale;
     a.limit_ns = kWaitLimitNs;

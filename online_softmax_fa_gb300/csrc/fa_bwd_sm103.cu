@@ -105,7 +105,9 @@ struct Params {
     const float *lse2;  // -LSE * log2(e)
     const float *dd;    // -D, D = rowsum(dO * O)
     int N, BH, n_blocks;
-    int head_group;  // causal CTA order: heads per group (see block_of)
+    int H, group;     // query heads per batch; query heads per K/V head
+    int grid_heads;   // heads the grid walks: K/V heads (dkdv) or query heads (dq)
+    int head_group;   // causal CTA order: heads per group (see block_of)
     float scale, scale_log2;
     uint64_t limit_ns;
 };
@@ -336,7 +338,7 @@ __device__ __forceinline__ void block_of(const Params &p, int &bh, int &blk) {
         const int grp = x / per_group;
         const int in = x - grp * per_group;
         const int h0 = grp * p.head_group;
-        const int gsize = min(p.head_group, p.BH - h0);  // the last group may be smaller
+        const int gsize = min(p.head_group, p.grid_heads - h0);  // the last group may be smaller
         const int rank = in / gsize;
         bh = h0 + (in - rank * gsize);
         blk = KEY_BLOCKS ? rank : p.n_blocks - 1 - rank;
@@ -346,6 +348,18 @@ __device__ __forceinline__ void block_of(const Params &p, int &bh, int &blk) {
     }
 }
 
+// Grouped-query attention: query head q_head(p, kv, g) is member g of K/V
+// head kv's group (query head h of a batch uses K/V head h / group).
+__device__ __forceinline__ int q_head(const Params &p, int kv, int g) {
+    const int hkv = p.H / p.group;  // K/V heads per batch
+    const int b = kv / hkv;
+    return b * p.H + (kv - b * hkv) * p.group + g;
+}
+__device__ __forceinline__ int kv_head(const Params &p, int bh) {
+    const int b = bh / p.H;
+    return b * (p.H / p.group) + (bh - b * p.H) / p.group;
+}
+
 // ============================== dK / dV kernel ==============================
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUtensorMap *tmK,
@@ -353,36 +367,36 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
                                             const Params &p, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    int bh, jb;  // jb: key block
+    int bh, jb;  // bh: K/V head; jb: key block
     block_of<CAUSAL, true>(p, bh, jb);
-    const int N = p.N;
     const int i0 = CAUSAL ? jb : 0;          // first query block touching this key block
-    const int n_q = p.n_blocks - i0;
-    const uint32_t tmem = *v.tmem_slot;
+    const int n_q = p.n_blocks - i0;         // query blocks per query head
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
-    (void)N, (void)tmem, (void)bh;
-    // ---- producer: K_j, V_j once; per query block Q_i, dO_i (TMA) and
-    // the block's LSE2 and D rows (bulk copies of the padded rows), all
-    // completing the stage's barrier
+    // ---- producer: K_j, V_j once; then, for each query head of the K/V
+    // head's group in turn, per query block Q_i, dO_i (TMA) and the block's
+    // LSE2 and D rows (bulk copies of the padded rows), all completing the
+    // stage's barrier
     if (lane == 0) {
         const uint64_t pol = l2_policy_evict_last();
         mbar_arrive_expect_tx(v.once, 2 * C::kTile);
         load_tile<D>(v.a, tmK, v.once, jb * kBlk, bh, pol);
         load_tile<D>(v.b, tmV, v.once, jb * kBlk, bh, pol);
-        const size_t prow = static_cast<size_t>(bh) * p.n_blocks * kBlk;
         int issued = 0;
         bool ok = true;
-        for (int t = 0; t < n_q && ok; ++t) {
+        for (int t = 0; t < p.group * n_q && ok; ++t) {
             const int s = t % C::kStages;
             if (t >= C::kStages)
                 ok = mbar_wait(&v.empty[s], ((t / C::kStages) & 1) ^ 1, ctl, kSiteEmpty);
             if (!ok) break;
-            const int q0 = (i0 + t) * kBlk;
+            const int g = t / n_q;
+            const int q0 = (i0 + t - g * n_q) * kBlk;
+            const int bq = q_head(p, bh, g);
+            const size_t prow = static_cast<size_t>(bq) * p.n_blocks * kBlk;
             float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
             uint8_t *st = v.ring + s * 2 * C::kTile;
             mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile + 2 * kBlk * 4);
-            load_tile<D>(st, tmQ, &v.full[s], q0, bh, pol);
-            load_tile<D>(st + C::kTile, tmdO, &v.full[s], q0, bh, pol);
+            load_tile<D>(st, tmQ, &v.full[s], q0, bq, pol);
+            load_tile<D>(st + C::kTile, tmdO, &v.full[s], q0, bq, pol);
             bulk_load(lse2, p.lse2 + prow + q0, kBlk * 4, &v.full[s], pol);
             bulk_load(dd, p.dd + prow + q0, kBlk * 4, &v.full[s], pol);
             ++issued;
@@ -415,7 +429,7 @@ __device__ __forceinline__ void dkdv_issue_sdp(const Params &p) {
     int bh, jb;  // jb: key block
     block_of<CAUSAL, true>(p, bh, jb);
     const int i0 = CAUSAL ? jb : 0;
-    const int n_u = 2 * (p.n_blocks - i0);  // 64-query halves
+    const int n_u = 2 * p.group * (p.n_blocks - i0);  // 64-query halves
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     (void)bh;
@@ -458,7 +472,7 @@ __device__ __forceinline__ void dkdv_issue_acc(const Params &p) {
     int bh, jb;  // jb: key block
     block_of<CAUSAL, true>(p, bh, jb);
     const int i0 = CAUSAL ? jb : 0;
-    const int n_u = 2 * (p.n_blocks - i0);
+    const int n_u = 2 * p.group * (p.n_blocks - i0);
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     (void)bh;
@@ -491,11 +505,12 @@ template <int D, bool CAUSAL>
 __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int lane) {
     using C = Cfg<D>;
     const View<D> v = view<D>();
-    int bh, jb;  // jb: key block
+    int bh, jb;  // bh: K/V head; jb: key block
     block_of<CAUSAL, true>(p, bh, jb);
     const int N = p.N;
     const int i0 = CAUSAL ? jb : 0;  // first query block touching this key block
-    const int n_u = 2 * (p.n_blocks - i0);
+    const int n_q = p.n_blocks - i0;  // query blocks per query head of the group
+    const int n_u = 2 * p.group * n_q;
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     // ---- elementwise: thread = key row of this block (TMEM lane); warp
@@ -512,7 +527,8 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
         // columns of them go to registers before S^T / dP^T are waited for
         ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
         if (!ok) break;
-        const int q0 = (i0 + t) * kBlk;
+        const int qi = t % n_q;  // query block within the current query head
+        const int q0 = (i0 + qi) * kBlk;
         const int cb = 64 * h + 32 * c;  // this warp's first column within the block
         const float *lse2 = v.rows + s * 2 * kBlk + cb, *dd = lse2 + kBlk;
         float4 l4[8], d4[8];
@@ -532,7 +548,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
         const uint32_t tp = tmem + lb + C::kTmP + 64 * h + 32 * c;
         tmem_ld32x2(ts, tp, sv, dv);
         // masked only on the diagonal block (causal) and a ragged last block
-        const bool masked = (CAUSAL && t == 0) || q0 + kBlk > N;
+        const bool masked = (CAUSAL && qi == 0) || q0 + kBlk > N;
         if (masked)
             p_ds_masked(sv, dv, lse2, dd, true, 0.f, 0.f, p.scale_log2, lim_lo, lim_hi, cb, pp,
                         pds);
@@ -633,6 +649,7 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     const uint32_t tmem = *v.tmem_slot;
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     (void)N, (void)tmem, (void)bh;
+    const int bk = kv_head(p, bh);  // this query head's K/V head
     if (lane == 0) {
         const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
         mbar_arrive_expect_tx(v.once, 2 * C::kTile);
@@ -646,13 +663,13 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
                 ok = mbar_wait(&v.empty[sk], ((t / C::kStagesK) & 1) ^ 1, ctl, kSiteEmpty);
             if (!ok) break;
             mbar_arrive_expect_tx(&v.full[sk], C::kTile);
-            load_tile<D>(v.ring + sk * C::kTile, tmK, &v.full[sk], t * kBlk, bh, pol_kv);
+            load_tile<D>(v.ring + sk * C::kTile, tmK, &v.full[sk], t * kBlk, bk, pol_kv);
             ++nk;
             if (t >= C::kStagesV)
                 ok = mbar_wait(&v.vempty[sv], ((t / C::kStagesV) & 1) ^ 1, ctl, kSiteEmpty);
             if (!ok) break;
             mbar_arrive_expect_tx(&v.vfull[sv], C::kTile);
-            load_tile<D>(v.vring + sv * C::kTile, tmV, &v.vfull[sv], t * kBlk, bh, pol_kv);
+            load_tile<D>(v.vring + sv * C::kTile, tmV, &v.vfull[sv], t * kBlk, bk, pol_kv);
             ++nv;
         }
         mbar_wait_drain(v.once, 0, p.limit_ns);
@@ -923,6 +940,8 @@ static int launch_bwd_t(const BwdArgs &a) {
     p.dd = dd;
     p.N = a.N;
     p.BH = a.BH;
+    p.H = a.H;
+    p.group = a.H / a.Hkv;
     p.n_blocks = n_blocks;
     p.scale = a.scale;
     p.scale_log2 = a.scale * bwd::kLog2e;
@@ -933,20 +952,26 @@ static int launch_bwd_t(const BwdArgs &a) {
     // + 1) heads.
     int sms = 0;
     FA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    {
-        const long long g = (3LL * (sms > 0 ? sms : 1) + n_blocks) / (n_blocks + 1);
-        p.head_group = static_cast<int>(g < 1 ? 1 : (g > a.BH ? a.BH : g));
-    }
-    const long long grid = static_cast<long long>(p.n_blocks) * a.BH;
-    if (grid > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
+    const long long hg = (3LL * (sms > 0 ? sms : 1) + n_blocks) / (n_blocks + 1);
+    const auto set_heads = [&](long long heads) {
+        p.grid_heads = static_cast<int>(heads);
+        p.head_group = static_cast<int>(hg < 1 ? 1 : (hg > heads ? heads : hg));
+        return static_cast<long long>(p.n_blocks) * heads;
+    };
+    const long long bh_kv = a.BH / p.group;
+    if (static_cast<long long>(p.n_blocks) * a.BH > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
+    // dK / dV: one CTA per (K/V head, key block)
+    const long long grid1 = set_heads(bh_kv);
     p.g0 = static_cast<__nv_bfloat16 *>(a.dK);
     p.g1 = static_cast<__nv_bfloat16 *>(a.dV);
-    k1<<<static_cast<unsigned>(grid), bwd::kThreads, C::kSmemBytes, a.stream>>>(
+    k1<<<static_cast<unsigned>(grid1), bwd::kThreads, C::kSmemBytes, a.stream>>>(
         *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, p);
     FA_CUDA_TRY(cudaGetLastError());
+    // dQ: one CTA per (query head, query block)
+    const long long grid2 = set_heads(a.BH);
     p.g0 = static_cast<__nv_bfloat16 *>(a.dQ);
     p.g1 = nullptr;
-    k2<<<static_cast<unsigned>(grid), bwd::kThreads, C::kSmemBytes, a.stream>>>(
+    k2<<<static_cast<unsigned>(grid2), bwd::kThreads, C::kSmemBytes, a.stream>>>(
         *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, p);
     FA_CUDA_TRY(cudaGetLastError());
     return FA_OK;

@@ -35,8 +35,10 @@ struct BwdArgs {
     const void *O, *dO;          // bf16 [BH, N, d]
     const float *LSE;            // fp32 [BH, N] (natural log)
     float *rows;                 // fp32 scratch [2][BH][Npad]: LSE*log2(e), rowsum(dO*O)
-    void *dQ, *dK, *dV;          // bf16 [BH, N, d]
+    void *dQ;                    // bf16 [BH, N, d]
+    void *dK, *dV;               // bf16 [BH / (H / Hkv), N, d]
     int BH, N, d;
+    int H, Hkv;                  // query and K/V heads per batch (Hkv divides H)
     bool causal;
     float scale;
     uint64_t limit_ns;

@@ -52,6 +52,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_bwd_workspace_bytes.restype = S
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, S, I, I, I, I, I, F, P]
     lib.fa_bwd.restype = I
+    lib.fa_bwd_gqa.argtypes = [P, P, P, P, P, P, P, P, P, P, S, I, I, I, I, I, I, F, P]
+    lib.fa_bwd_gqa.restype = I
     lib.fa_decode_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.fa_decode_workspace_bytes.restype = S
     lib.fa_decode.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
@@ -194,6 +196,40 @@ def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, workspace=None,
                                1 if causal else 0, float(scale), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_gqa(q, k, v, o, lse, do, dq=None, dk=None, dv=None, workspace=None,
+               causal: bool = False, scale: float | None = None, stream=None):
+    """Gradients of fa_fwd_gqa: q, o, do [B, H, N, d]; k, v [B, H_kv, N, d]
+    with H_kv dividing H; lse [B, H, N].  Returns (dq [B, H, N, d],
+    dk, dv [B, H_kv, N, d]), allocated when not given."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda \
+                or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 [B, H, N, d] tensor")
+    B, H, N, d = (int(x) for x in q.shape)
+    if o.shape != q.shape or do.shape != q.shape:
+        raise ValueError("o and do must be shaped like q")
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    H_kv = int(k.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    rc = load_library().fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), B, H, H_kv, N,
+                                   d, 1 if causal else 0, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_gqa")
     return dq, dk, dv
 
 

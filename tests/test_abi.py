@@ -136,6 +136,16 @@ def test_gqa_argument_checks(lib):
     assert lib.fa_fwd_gqa(*base, 1, 8, 2, 8, 96, 0, 0.125, None) == -3
 
 
+def test_bwd_gqa_argument_checks(lib):
+    # Q K V O dO LSE dQ dK dV workspace bytes
+    base = (16, 32, 48, 64, 80, 96, 4096, 8192, 12288, 65536, 1 << 30)
+    # H_kv must divide H and be >= 1; head dimension 64 or 128; null pointers
+    assert lib.fa_bwd_gqa(*base, 1, 8, 3, 8, 64, 0, 0.125, None) == -2
+    assert lib.fa_bwd_gqa(*base, 1, 8, 0, 8, 64, 0, 0.125, None) == -2
+    assert lib.fa_bwd_gqa(*base, 1, 8, 2, 8, 256, 0, 0.0625, None) == -3
+    assert lib.fa_bwd_gqa(None, *base[1:], 1, 8, 2, 8, 64, 0, 0.125, None) == -1
+
+
 def test_decode_argument_checks(lib):
     need = lib.fa_decode_workspace_bytes(2, 8, 2, 1000, 128)
     assert need > 0 and need % 256 == 0
