@@ -82,7 +82,8 @@ struct Cfg {
     static constexpr int kOffVq = kOffRing + kStagesK * kTile;      // dq: V ring
     static constexpr int kOffBar = kOffRing + (kRingDkdv > kRingDq ? kRingDkdv : kRingDq);
     // once, full/empty[3] (dkdv: stages; dq: K ring), vfull/vempty[2] (dq: V
-    // ring), s_full[2], p_full[2], o_full, dp_free
+    // ring; dkdv: vfull[2] = buf_free of the two S^T/dP^T half buffers),
+    // s_full[2], p_full[2], o_full, dp_free (dq)
     static constexpr int kNumBars = 1 + 2 * 3 + 2 * 2 + 6;
     static_assert(kStages <= 3 && kStagesK <= 3 && kStagesV <= 2, "barrier slots");
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
