@@ -138,6 +138,7 @@ struct Params {
     int n_items;    // BH x n_qblocks
     float scale_log2;  // scale * log2(e)
     uint64_t limit_ns;
+    int o_align32;     // O is 32-byte aligned: the epilogue stores 32 bytes at a time
 };
 
 // Shared-memory layout of one CTA (rebuilt where needed: it costs a few
@@ -527,10 +528,18 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
                 pk[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l,
                                     __uint_as_float(o[2 * t + 1]) * inv_l);
             if (in_range) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+                if (p.o_align32) {
+                    st_global_v8(orow + 32 * c, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6],
+                                 pk[7]);
+                    st_global_v8(orow + 32 * c + 16, pk[8], pk[9], pk[10], pk[11], pk[12],
+                                 pk[13], pk[14], pk[15]);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+                    for (int t = 0; t < 4; ++t)
+                        dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2],
+                                            pk[4 * t + 3]);
+                }
             }
         }
         // O_k is read out: the next item's first PV_k may overwrite it.
@@ -670,6 +679,7 @@ static int launch_t(const LaunchArgs &a) {
     p.n_items = static_cast<int>(items);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
+    p.o_align32 = (reinterpret_cast<uintptr_t>(a.O) & 31u) == 0 ? 1 : 0;
     // one persistent CTA per SM (the shared-memory footprint allows one)
     const int grid = static_cast<int>(items < sms ? items : sms);
     kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, p);

@@ -403,6 +403,16 @@ __device__ __forceinline__ void regs_decrease() {
 }
 
 // ------------------------------------------------------------------- math
+// 32 bytes to global memory in one store (the address must be 32-byte
+// aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // Hardware base-2 exponential (MUFU), flush-to-zero; ex2(-inf) = +0.
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

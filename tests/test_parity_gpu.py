@@ -415,6 +415,23 @@ from online_softmax_fa_gb300.inputs import make_grad  # noqa: E402
 G_MAX_REL, G_MEAN_REL, G_FLOOR = 2e-2, 1e-2, 1e-3
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_only_16_byte_aligned(fa, d):
+    """O 16-byte but not 32-byte aligned (the API's minimum): the epilogue
+    takes its 16-byte stores and writes the same bits as with an aligned O."""
+    q, k, v = make_qkv(1, 3, 300, d, seed=90 + d)
+    dev = torch.device("cuda")
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o_ref, l_ref = fa.fa_fwd(qd, kd, vd, causal=True)
+    flat = torch.empty(o_ref.numel() + 8, dtype=torch.bfloat16, device=dev)
+    o_off = flat[8:].view(o_ref.shape)  # 16 bytes past a 256-byte aligned base
+    assert o_off.data_ptr() % 32 == 16
+    o2, l2 = fa.fa_fwd(qd, kd, vd, o=o_off, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == 0
+    assert torch.equal(o2, o_ref) and torch.equal(l2, l_ref)
+
+
 def _bwd_run(fa, q, k, v, do, causal, scale):
     dev = torch.device("cuda")
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
