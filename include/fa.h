@@ -42,7 +42,7 @@ typedef enum {
     FA_ERR_ARCH = -5,        /* current device is not compute capability 10.3 */
     FA_ERR_LAUNCH = -6,      /* a CUDA call failed (launch, copy, tensor map) */
     FA_ERR_TIMEOUT = -7,     /* a kernel wait exceeded its limit (see fa_device_error) */
-    FA_ERR_UNSUPPORTED = -8, /* valid request this build does not implement */
+    FA_ERR_UNSUPPORTED = -8, /* valid request this library does not implement */
     FA_ERR_SCALE = -9,       /* scale is not a finite number > 0 */
     FA_ERR_ALIAS = -10,      /* an output buffer overlaps an input buffer */
     FA_ERR_WORKSPACE = -11   /* workspace too small or misaligned */

@@ -555,7 +555,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
         case FA_ERR_LAUNCH: return "a CUDA call failed";
         case FA_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
-        case FA_ERR_UNSUPPORTED: return "request not supported by this build";
+        case FA_ERR_UNSUPPORTED: return "request not supported by this library";
         case FA_ERR_SCALE: return "scale must be a finite number > 0";
         case FA_ERR_ALIAS: return "an output buffer overlaps an input buffer";
         case FA_ERR_WORKSPACE: return "workspace NULL, too small or not 256-byte aligned";
