@@ -13,22 +13,26 @@
 //   * pre:  D = rowsum(dO * O) in fp32 and LSE * log2(e), one warp per row,
 //           into rows padded to a multiple of 128 per head (the workspace)
 //           so that the dkdv producer fetches a block's rows with bulk copies.
-//   * dkdv: one CTA per (b, h, 128-key block j), query blocks i as the inner
-//           loop, each taken in two 64-query halves.  On tcgen05 with TMEM
+//   * dkdv: one CTA per (b, K/V head, 128-key block j), the query blocks i
+//           of every query head of the K/V head's group as the inner loop
+//           (one head per group without grouped-query attention), each
+//           taken in two 64-query halves.  On tcgen05 with TMEM
 //           accumulators: S^T = K_j Q_h^T and dP^T = V_j dO_h^T (keys are
 //           the MMA rows) for one half while eight elementwise warps
 //           (thread = key row = TMEM lane, two warps per row, 32 columns
 //           each) form P^T and dS^T in bf16 for the previous half, then
 //           dV_j += P^T dO_h and dK_j += dS^T Q_h read them from TMEM.
 //           Two warps issue the MMAs: one S^T / dP^T, one dV / dK.
-//   * dq:   one CTA per (b, h, 128-query block i), key blocks j inner:
+//   * dq:   one CTA per (b, h, 128-query block i), key blocks j of K/V head
+//           h / group inner:
 //           S = Q_i K_j^T and dP = dO_i V_j^T, then dS (thread = query row),
 //           then dQ_i += dS K_j; S is double-buffered, so the next block's S
 //           and dP run on the tensor pipe while the warps work on this one.
 // Causal: blocks entirely above the diagonal are skipped; the diagonal block
 // is masked.  Causal CTAs run in cost order (heaviest first) within groups
-// of heads small enough to share L2.  TMEM (dkdv): S^T of the two halves at [0,64) and [64,128), dP^T
-// at [128,192) and [192,256), dV [256,256+d), dK [256+d, 256+2d); P^T and
+// of heads small enough to share L2.  TMEM (dkdv): S^T of the two halves at
+// [0,64) and [64,128), dP^T at [128,192) and [192,256), dV [256,256+d),
+// dK [256+d, 256+2d); P^T and
 // dS^T of a half are bf16 pairs over its S^T columns, each column-half warp
 // writing over its own 32 columns (P^T over the first 16, dS^T over the
 // next 16).  TMEM (dq): S [0,128) and [128,256), dP [256,384), dQ [384,384+d).
