@@ -305,7 +305,8 @@ def run_ours(args, w, causal):
     if status != 0:
         raise RuntimeError(f"device status {status} during the timed region")
     total_ms = e0.elapsed_time(e1)
-    kern_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = statistics.fmean(launch_ms)
     total_ms_max = max_over_ranks(total_ms, ws)
     value = aggregate_tflops(flops, args.steps, total_ms_max, ws)
 
@@ -352,7 +353,10 @@ def run_ours(args, w, causal):
                      "peak_source": f"bf16_tflops (burst) of {peak_kind}",
                      "traffic": recorded_traffic() if w.name == "llama" else None,
                      "kernel": f"fa_fwd_kernel<{d},{str(causal).lower()}>",
-                     "kernel_ms": kern_ms},
+                     "kernel_ms": kern_ms,
+                     # per-launch CUDA-event durations of the same timed launches
+                     "kernel_ms_median": statistics.median(launch_ms),
+                     "kernel_ms_min": min(launch_ms), "launches_timed": len(launch_ms)},
         "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                  "ms_per_step": e2e_ms / e2e_steps,
