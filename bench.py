@@ -201,6 +201,24 @@ def oracle_inputs(w):
     return tuple(oracle.bf16_bits_to_f64(t.reshape(shp)) for t in (q, k, v))
 
 
+def host_cpu() -> str:
+    """The host CPU as the kernel reports it (model name or CPU part), with
+    the machine type and the number of online cores."""
+    import platform
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part") and ":" in line:
+                    name = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return f"{platform.machine()} {name} x{os.cpu_count()}".strip()
+
+
 def cpu_baseline(w, causal, target_s=15.0):
     import oracle
     qf, kf, vf = oracle_inputs(w)
@@ -210,6 +228,7 @@ def cpu_baseline(w, causal, target_s=15.0):
     rph = int(min(w.N, max(8, target_s / max(per_row, 1e-6))))
     dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+            "cpu": host_cpu(),
             "sample": f"{rph} evenly spaced query rows in each of the {w.B * w.H} heads "
                       f"({rph * w.B * w.H} rows, {dt:.1f} s); fp64, S and P materialised "
                       f"over all N keys per row; FLOPs counted as 4*d per attended key"}
@@ -243,6 +262,7 @@ def run_reference(args, w, causal):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": workload_config(w, causal),
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+                            "cpu": host_cpu(),
                             "sample": sample},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
