@@ -331,32 +331,36 @@ def run_ours(args, w, causal):
     value = aggregate_tflops(flops, args.steps, total_ms_max, ws)
 
     # end to end through the host-buffer entry point: H2D of Q, K, V from
-    # pinned memory, the kernel, D2H of O and LSE -- every step (the
-    # host-buffer entry point covers equal query and K/V head counts)
-    e2e_steps = max(3, min(args.steps, 30)) if not gqa else 0
+    # pinned memory, the kernel, D2H of O and LSE -- every step
+    e2e_steps = max(3, min(args.steps, 30))
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty_like(q).pin_memory()
     lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    wsp = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8,
-                      device=dev)
-    for _ in range(2 if e2e_steps else 0):
-        fa.fa_fwd_host(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
+    if gqa:
+        wsp = torch.empty(fa.fa_fwd_host_gqa_workspace_bytes(B, H, w.kv_heads, N, d),
+                          dtype=torch.uint8, device=dev)
+        host_step = fa.fa_fwd_host_gqa
+    else:
+        wsp = torch.empty(fa.fa_fwd_host_workspace_bytes(B, H, N, d), dtype=torch.uint8,
+                          device=dev)
+        host_step = fa.fa_fwd_host
+    for _ in range(2):
+        host_step(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
     barrier(ws)
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(stream)
     for _ in range(e2e_steps):
-        fa.fa_fwd_host(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
+        host_step(qh, kh, vh, oh, lh, wsp, causal=causal, scale=w.scale)
     x1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     if fa.fa_device_error() != 0:
         raise RuntimeError("device status set during the end-to-end leg")
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), ws)
-    e2e_value = aggregate_tflops(flops, e2e_steps, e2e_ms, ws) if e2e_steps else None
-    tbytes = q.numel() * 2
-    h2d = 3 * tbytes
-    d2h = tbytes + B * H * N * 4
+    e2e_value = aggregate_tflops(flops, e2e_steps, e2e_ms, ws)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = q.numel() * 2 + B * H * N * 4
 
     if rank != 0:
         return
@@ -377,10 +381,11 @@ def run_ours(args, w, causal):
                      # per-launch CUDA-event durations of the same timed launches
                      "kernel_ms_median": statistics.median(launch_ms),
                      "kernel_ms_min": min(launch_ms), "launches_timed": len(launch_ms)},
-        "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                 "ms_per_step": e2e_ms / e2e_steps,
-                 "api": "fa_fwd_host (C ABI, pinned host buffers)"} if e2e_steps else None),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": e2e_ms / e2e_steps,
+                "api": ("fa_fwd_host_gqa" if gqa else "fa_fwd_host")
+                       + " (C ABI, pinned host buffers)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

@@ -105,7 +105,7 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * asynchronously with respect to the host and ordered after the earlier work
  * on `stream` (synchronise `stream` before reading O_host / LSE_host).  The
  * heads are cut into chunks whose copy-in, kernel and copy-out overlap on
- * three streams the library creates once per device (and keeps); calls that
+ * four streams the library creates once per device (and keeps); calls that
  * use them are enqueued one at a time.  The results equal those of one
  * fa_fwd call.  Host buffers should be pinned for the copies to overlap;
  * pageable memory works but the copies then block the host.
@@ -117,12 +117,43 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
  *                           fa_fwd_host_workspace_bytes(B, H, N, d) bytes,
  *                           256-byte aligned; contents are scratch.
  * Other arguments and errors as fa_fwd; FA_ERR_WORKSPACE if the workspace
- * is NULL, too small or misaligned.
+ * is NULL, too small or misaligned.  Argument errors are found before
+ * anything is enqueued.  A CUDA failure found part-way (a copy or launch the
+ * runtime refuses after earlier chunks were enqueued) returns its error
+ * with `stream` made to wait for everything already enqueued, so the host
+ * and device buffers may be released once `stream` is synchronised; the
+ * outputs are then undefined.
  */
 int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host,
                 void *O_host, float *LSE_host, void *workspace,
                 size_t workspace_bytes, int B, int H, int N, int d,
                 int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_fwd_host_gqa_workspace_bytes -- device workspace fa_fwd_host_gqa needs:
+ * Q and O ([B, H, N, d] bf16), K and V ([B, H_kv, N, d] bf16) and LSE
+ * ([B, H, N] fp32), each 256-byte aligned.  0 for an invalid shape or an
+ * H_kv that does not divide H.
+ */
+size_t fa_fwd_host_gqa_workspace_bytes(int B, int H, int H_kv, int N, int d);
+
+/*
+ * fa_fwd_host_gqa -- fa_fwd_gqa on host buffers ("Understanding
+ * FlashAttention Pt 1", section 4.1: H query heads share H_kv K/V heads):
+ *   Q_host, O_host  bf16 [B, H, N, d];  LSE_host fp32 [B, H, N]
+ *   K_host, V_host  bf16 [B, H_kv, N, d] (each K/V head copied in once for
+ *                   its whole group of query heads)
+ *   workspace       at least fa_fwd_host_gqa_workspace_bytes(B, H, H_kv, N, d)
+ *                   bytes of device memory, 256-byte aligned
+ * A chunk holds whole groups (a K/V head with all its query heads).  The
+ * results equal those of one fa_fwd_gqa call.  Everything else, including
+ * errors and the part-way failure rule, as fa_fwd_host; fa_fwd_host is this
+ * call with H_kv = H.
+ */
+int fa_fwd_host_gqa(const void *Q_host, const void *K_host, const void *V_host,
+                    void *O_host, float *LSE_host, void *workspace,
+                    size_t workspace_bytes, int B, int H, int H_kv, int N, int d,
+                    int causal, float scale, fa_stream_t stream);
 
 /*
  * fa_bwd_workspace_bytes -- device workspace fa_bwd needs: two fp32 per
@@ -230,9 +261,11 @@ int fa_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
  *     fa_decode_workspace_bytes(B, H, H_kv, N, d) > 16 MiB, return
  *     FA_ERR_WORKSPACE (fa_last_error_detail says why) and enqueue nothing.
  *   - Allocates nothing, on the host or the device.
- *   - The first call on each device looks up the area's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture.
+ *   - The area's device address belongs to the CUDA context: the first
+ *     call in each context (per device, with that device current) looks it
+ *     up without allocating and caches it with the context's unique id; a
+ *     later call in another context, or after cudaDeviceReset(), looks it up
+ *     again.  Make that first call in a context before any stream capture.
  *   - Every call shares the one area: calls that overlap on the GPU (other
  *     streams, other host threads) race and must be ordered by the caller.
  *     Nothing in it has to start at zero: each call writes every state it

@@ -14,11 +14,12 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "host_pipe.h"
 
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per in-kernel wait
-constexpr int kMaxDevices = 64;
+using fa::kMaxDevices;
 
 std::atomic<int> g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 
@@ -114,6 +115,18 @@ thread_local char g_detail[256] = "";
 }  // namespace
 
 namespace fa {
+int device_sm_count(int dev) {
+    static std::atomic<int> counts[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    int n = counts[dev].load(std::memory_order_acquire);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        counts[dev].store(n, std::memory_order_release);
+    }
+    return n;
+}
+
 int record_cuda_error(cudaError_t e, const char *what) {
     std::snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", what, cudaGetErrorName(e),
                   cudaGetErrorString(e));
@@ -177,11 +190,17 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int
     return fa_fwd_gqa(Q, K, V, O, LSE, B, H, H, N, d, causal, scale, stream);
 }
 
-size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+size_t fa_fwd_host_gqa_workspace_bytes(int B, int H, int H_kv, int N, int d) {
     if (check_shape(B, H, N, d, 1.f, true) != FA_OK) return 0;
-    const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    if (H_kv < 1 || H % H_kv != 0) return 0;
+    const size_t q_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
     const size_t l_bytes = static_cast<size_t>(B) * H * N * 4;
-    return 4 * align256(t_bytes) + align256(l_bytes);
+    return 2 * align256(q_bytes) + 2 * align256(kv_bytes) + align256(l_bytes);
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+    return fa_fwd_host_gqa_workspace_bytes(B, H, H, N, d);
 }
 
 namespace {
@@ -196,7 +215,7 @@ struct HostPipe {
     cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
 };
-HostPipe g_pipes[64];
+HostPipe g_pipes[kMaxDevices];
 
 // Creates the device's streams and events on first use; call with h.mu held.
 int host_pipe_init(HostPipe &h) {
@@ -256,24 +275,28 @@ int plan_chunks(long long BH, long long equal_chunks, long long *bounds) {
 }
 }  // namespace
 
-int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
-                float *LSE_host, void *workspace, size_t workspace_bytes, int B, int H, int N,
-                int d, int causal, float scale, fa_stream_t stream) {
+int fa_fwd_host_gqa(const void *Q_host, const void *K_host, const void *V_host,
+                    void *O_host, float *LSE_host, void *workspace, size_t workspace_bytes,
+                    int B, int H, int H_kv, int N, int d, int causal, float scale,
+                    fa_stream_t stream) {
     if (!Q_host || !K_host || !V_host || !O_host || !LSE_host) return FA_ERR_NULL;
     int rc = check_shape(B, H, N, d, scale, true);
     if (rc != FA_OK) return rc;
-    const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
+    const size_t need = fa_fwd_host_gqa_workspace_bytes(B, H, H_kv, N, d);
     if (!workspace || workspace_bytes < need ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FA_ERR_WORKSPACE;
     rc = check_arch();
     if (rc != FA_OK) return rc;
-    const size_t t_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t q_bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
     uint8_t *w = static_cast<uint8_t *>(workspace);
-    uint8_t *dQ = w, *dK = dQ + align256(t_bytes), *dV = dK + align256(t_bytes);
-    uint8_t *dO = dV + align256(t_bytes);
-    float *dL = reinterpret_cast<float *>(dO + align256(t_bytes));
+    uint8_t *dQ = w, *dO = dQ + align256(q_bytes), *dK = dO + align256(q_bytes);
+    uint8_t *dV = dK + align256(kv_bytes);
+    float *dL = reinterpret_cast<float *>(dV + align256(kv_bytes));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int G = H / H_kv;  // query heads per K/V head
 
     // The heads are independent, so the work is cut into chunks of heads:
     // the copy-in of chunk c+1, the kernel on chunk c and the copy-out of
@@ -288,60 +311,103 @@ int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void
     FA_CUDA_TRY(cudaGetDevice(&dev));
     int sms = 0;
     FA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const long long BH = static_cast<long long>(B) * H;
+    // chunks are whole groups of query heads sharing a K/V head (bounds in
+    // K/V heads; a flattened query head x uses flattened K/V head x / G)
+    const long long BH = static_cast<long long>(B) * H, BHkv = BH / G;
     const long long rows_per_item = d == 256 ? 128 : 256;
     const long long qblocks = (static_cast<long long>(N) + rows_per_item - 1) / rows_per_item;
     long long equal = BH * qblocks / (sms > 0 ? sms : 1);
     if (equal > 8) equal = 8;
-    if (equal > BH) equal = BH;
+    if (equal > BHkv) equal = BHkv;
     if (equal < 1) equal = 1;
     long long bounds[HostPipe::kMaxChunks + 1];
-    const int chunks = plan_chunks(BH, equal, bounds);
-    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
+    const int chunks = plan_chunks(BHkv, equal, bounds);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
     HostPipe *hp = &g_pipes[dev];
     std::lock_guard<std::mutex> lock(hp->mu);
     rc = host_pipe_init(*hp);
     if (rc != FA_OK) return rc;
-    // everything below runs after the caller's earlier work on `stream`
-    FA_CUDA_TRY(cudaEventRecord(hp->start, s));
-    FA_CUDA_TRY(cudaStreamWaitEvent(hp->in, hp->start, 0));
-    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp[0], hp->start, 0));
-    FA_CUDA_TRY(cudaStreamWaitEvent(hp->comp[1], hp->start, 0));
-    FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->start, 0));
     const size_t head_t = static_cast<size_t>(N) * d * 2, head_l = static_cast<size_t>(N) * 4;
-    for (int c = 0; c < chunks; ++c) {
-        const long long h0 = bounds[c], h1 = bounds[c + 1];
-        cudaStream_t comp = hp->comp[c & 1];
-        const size_t off_t = h0 * head_t, n_t = (h1 - h0) * head_t;
-        const size_t off_l = h0 * head_l, n_l = (h1 - h0) * head_l;
-        FA_CUDA_TRY(cudaMemcpyAsync(dQ + off_t, static_cast<const uint8_t *>(Q_host) + off_t, n_t,
-                                    cudaMemcpyHostToDevice, hp->in));
-        FA_CUDA_TRY(cudaMemcpyAsync(dK + off_t, static_cast<const uint8_t *>(K_host) + off_t, n_t,
-                                    cudaMemcpyHostToDevice, hp->in));
-        FA_CUDA_TRY(cudaMemcpyAsync(dV + off_t, static_cast<const uint8_t *>(V_host) + off_t, n_t,
-                                    cudaMemcpyHostToDevice, hp->in));
-        FA_CUDA_TRY(cudaEventRecord(hp->loaded[c], hp->in));
-        FA_CUDA_TRY(cudaStreamWaitEvent(comp, hp->loaded[c], 0));
-        // one batch of h1 - h0 heads (B = 1): MHA heads need no batch index
-        rc = fa_fwd(dQ + off_t, dK + off_t, dV + off_t, dO + off_t,
-                    reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(dL) + off_l), 1,
-                    static_cast<int>(h1 - h0), N, d, causal, scale,
-                    reinterpret_cast<fa_stream_t>(comp));
-        if (rc != FA_OK) return rc;
-        FA_CUDA_TRY(cudaEventRecord(hp->computed[c], comp));
-        FA_CUDA_TRY(cudaStreamWaitEvent(hp->out, hp->computed[c], 0));
-        FA_CUDA_TRY(cudaMemcpyAsync(static_cast<uint8_t *>(O_host) + off_t, dO + off_t, n_t,
-                                    cudaMemcpyDeviceToHost, hp->out));
-        FA_CUDA_TRY(cudaMemcpyAsync(reinterpret_cast<uint8_t *>(LSE_host) + off_l,
-                                    reinterpret_cast<uint8_t *>(dL) + off_l, n_l,
-                                    cudaMemcpyDeviceToHost, hp->out));
-    }
-    // the caller's stream resumes once the last copy-out is done (the
-    // copy-out stream has waited for every kernel, in order, and each
-    // kernel for its copy-in)
-    FA_CUDA_TRY(cudaEventRecord(hp->done, hp->out));
-    FA_CUDA_TRY(cudaStreamWaitEvent(s, hp->done, 0));
-    return FA_OK;
+    // The stream operations of the pipeline (host_pipe.h holds its order).
+    // Chunk c covers K/V heads [bounds[c], bounds[c+1]) and their query
+    // heads [G bounds[c], G bounds[c+1]).
+    struct Ops {
+        HostPipe *hp;
+        cudaStream_t caller;
+        const long long *bounds;
+        long long G;
+        size_t head_t, head_l;
+        const uint8_t *Qh, *Kh, *Vh;
+        uint8_t *Oh, *Lh, *dQ, *dK, *dV, *dO, *dL;
+        int N, d, causal;
+        float scale;
+        cudaStream_t stream(fa::pipe::Stream s) const {
+            switch (s) {
+                case fa::pipe::kIn: return hp->in;
+                case fa::pipe::kComp0: return hp->comp[0];
+                case fa::pipe::kComp1: return hp->comp[1];
+                case fa::pipe::kOut: return hp->out;
+                default: return caller;
+            }
+        }
+        cudaEvent_t event(fa::pipe::Event e) const {
+            switch (e.kind) {
+                case fa::pipe::kStart: return hp->start;
+                case fa::pipe::kLoaded: return hp->loaded[e.chunk];
+                case fa::pipe::kComputed: return hp->computed[e.chunk];
+                default: return hp->done;
+            }
+        }
+        int record(fa::pipe::Event e, fa::pipe::Stream s) {
+            FA_CUDA_TRY(cudaEventRecord(event(e), stream(s)));
+            return FA_OK;
+        }
+        int wait(fa::pipe::Stream s, fa::pipe::Event e) {
+            FA_CUDA_TRY(cudaStreamWaitEvent(stream(s), event(e), 0));
+            return FA_OK;
+        }
+        int copy_in(int c) {
+            const size_t kv_off = bounds[c] * head_t, kv_n = (bounds[c + 1] - bounds[c]) * head_t;
+            FA_CUDA_TRY(cudaMemcpyAsync(dQ + G * kv_off, Qh + G * kv_off, G * kv_n,
+                                        cudaMemcpyHostToDevice, hp->in));
+            FA_CUDA_TRY(cudaMemcpyAsync(dK + kv_off, Kh + kv_off, kv_n, cudaMemcpyHostToDevice,
+                                        hp->in));
+            FA_CUDA_TRY(cudaMemcpyAsync(dV + kv_off, Vh + kv_off, kv_n, cudaMemcpyHostToDevice,
+                                        hp->in));
+            return FA_OK;
+        }
+        int launch(int c, fa::pipe::Stream s) {
+            // one batch of the chunk's heads (B = 1): query head i of the
+            // chunk uses its K/V head i / G, as in the whole problem
+            const long long hkv = bounds[c + 1] - bounds[c];
+            const size_t kv_off = bounds[c] * head_t, l_off = G * bounds[c] * head_l;
+            return fa_fwd_gqa(dQ + G * kv_off, dK + kv_off, dV + kv_off, dO + G * kv_off,
+                              reinterpret_cast<float *>(dL + l_off), 1,
+                              static_cast<int>(G * hkv), static_cast<int>(hkv), N, d, causal,
+                              scale, reinterpret_cast<fa_stream_t>(stream(s)));
+        }
+        int copy_out(int c) {
+            const long long hq = G * (bounds[c + 1] - bounds[c]);
+            const size_t q_off = G * bounds[c] * head_t, l_off = G * bounds[c] * head_l;
+            FA_CUDA_TRY(cudaMemcpyAsync(Oh + q_off, dO + q_off, hq * head_t,
+                                        cudaMemcpyDeviceToHost, hp->out));
+            FA_CUDA_TRY(cudaMemcpyAsync(Lh + l_off, dL + l_off, hq * head_l,
+                                        cudaMemcpyDeviceToHost, hp->out));
+            return FA_OK;
+        }
+    } ops{hp, s, bounds, G, head_t, head_l,
+          static_cast<const uint8_t *>(Q_host), static_cast<const uint8_t *>(K_host),
+          static_cast<const uint8_t *>(V_host), static_cast<uint8_t *>(O_host),
+          reinterpret_cast<uint8_t *>(LSE_host), dQ, dK, dV, dO,
+          reinterpret_cast<uint8_t *>(dL), N, d, causal, scale};
+    return fa::pipe::run(ops, chunks);
+}
+
+int fa_fwd_host(const void *Q_host, const void *K_host, const void *V_host, void *O_host,
+                float *LSE_host, void *workspace, size_t workspace_bytes, int B, int H, int N,
+                int d, int causal, float scale, fa_stream_t stream) {
+    return fa_fwd_host_gqa(Q_host, K_host, V_host, O_host, LSE_host, workspace,
+                           workspace_bytes, B, H, H, N, d, causal, scale, stream);
 }
 
 // ----------------------------------------------------------- decoding
@@ -430,18 +496,24 @@ int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, floa
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
     int rc = check_decode_shape(B, H, H_kv, N, d, scale);
     if (rc != FA_OK) return rc;
-    size_t acc_bytes = 0, ml_bytes = 0;
-    decode_layout(B, H, H_kv, N, d, &acc_bytes, &ml_bytes);
-    if (acc_bytes + ml_bytes > (static_cast<size_t>(16) << 20))
-        return fa::record_message(FA_ERR_WORKSPACE,
-                                  "request needs more than the 16 MiB of library-owned "
-                                  "decoding scratch; use fa_decode with a workspace");
     rc = check_arch();
     if (rc != FA_OK) return rc;
+    // the area's device address in the current context (looked up, without
+    // allocating, on the first call in each context) and its size
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
     rc = fa::decode_static_scratch(&scratch, &scratch_bytes);
     if (rc != FA_OK) return rc;
+    size_t acc_bytes = 0, ml_bytes = 0;
+    decode_layout(B, H, H_kv, N, d, &acc_bytes, &ml_bytes);
+    if (acc_bytes + ml_bytes > scratch_bytes) {
+        char msg[200];
+        std::snprintf(msg, sizeof msg,
+                      "request needs %zu bytes of decoding scratch, more than the %zu MiB "
+                      "the library owns; use fa_decode with a workspace",
+                      acc_bytes + ml_bytes, scratch_bytes >> 20);
+        return fa::record_message(FA_ERR_WORKSPACE, msg);
+    }
     // Same checks and kernels as the caller-workspace entry point.
     return fa_decode(Q, K, V, O, LSE, scratch, scratch_bytes, B, H, H_kv, N, d, scale, stream);
 }
@@ -550,7 +622,9 @@ const char *fa_status_string(int status) {
         case FA_OK: return "ok";
         case FA_ERR_NULL: return "a required pointer is NULL";
         case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and fit the indexing)";
-        case FA_ERR_HEADDIM: return "head dimension d must be 64 or 128";
+        case FA_ERR_HEADDIM:
+            return "head dimension not supported by this entry point (64 and 128; "
+                   "also 256 for the forward and decoding)";
         case FA_ERR_ALIGN: return "Q, K, V, O must be 16-byte aligned and LSE 4-byte aligned";
         case FA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
         case FA_ERR_LAUNCH: return "a CUDA call failed";

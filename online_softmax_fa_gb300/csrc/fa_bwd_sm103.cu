@@ -917,19 +917,15 @@ __global__ void pre_kernel(const __nv_bfloat16 *__restrict__ O,
 template <int D, bool CAUSAL>
 static int launch_bwd_t(const BwdArgs &a) {
     using C = bwd::Cfg<D>;
-    static int configured[64] = {0};
+    static std::atomic<int> configured1[kMaxDevices], configured2[kMaxDevices];
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
     auto k1 = bwd::dkdv_kernel<D, CAUSAL>;
     auto k2 = bwd::dq_kernel<D, CAUSAL>;
-    if (!configured[dev]) {
-        FA_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-        FA_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-        configured[dev] = 1;
-    }
+    int rc = set_smem_once(configured1, dev, k1, C::kSmemBytes);
+    if (rc == FA_OK) rc = set_smem_once(configured2, dev, k2, C::kSmemBytes);
+    if (rc != FA_OK) return rc;
     const int n_blocks = (a.N + bwd::kBlk - 1) / bwd::kBlk;
     const int Npad = n_blocks * bwd::kBlk;
     const long long rows_pad = static_cast<long long>(a.BH) * Npad;
@@ -955,8 +951,7 @@ static int launch_bwd_t(const BwdArgs &a) {
     // CTAs (about 2 / (n_blocks + 1) of a head's work each) start well
     // before the end even when the group runs last: about 3 x SMs / (n_blocks
     // + 1) heads.
-    int sms = 0;
-    FA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int sms = device_sm_count(dev);
     const long long hg = (3LL * (sms > 0 ? sms : 1) + n_blocks) / (n_blocks + 1);
     const auto set_heads = [&](long long heads) {
         p.grid_heads = static_cast<int>(heads);

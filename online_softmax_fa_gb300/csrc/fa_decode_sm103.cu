@@ -479,32 +479,17 @@ size_t decode_state_count(int B, int H, int H_kv) {
     return static_cast<size_t>(heads) * dec_slots(heads, kDecMaxGrid) * (H / H_kv);
 }
 
-static int dec_sm_count(int dev) {
-    static int counts[64] = {0};
-    if (dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
-}
-
 template <int D, int G>
 static int launch_decode_t(const DecodeArgs &a) {
     using C = DecCfg<D, G>;
     auto kern = fa_decode_split_kernel<D, G>;
-    static int configured[64] = {0};
+    static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
-    if (!configured[dev]) {
-        FA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-        configured[dev] = 1;
-    }
-    const int sms = dec_sm_count(dev);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
+    const int rc = set_smem_once(configured, dev, kern, C::kSmemBytes);
+    if (rc != FA_OK) return rc;
+    const int sms = device_sm_count(dev);
     if (sms <= 0) return record_message(FA_ERR_LAUNCH, "cannot query the SM count");
     const int heads = a.B * a.H_kv;
     const int T_h = (a.N + C::kTileKeys - 1) / C::kTileKeys;
@@ -575,24 +560,64 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 namespace {
+// The device address of g_decode_scratch belongs to a CUDA context: a
+// device reset, or another context made current on the same device, gives
+// the module a new copy.  Each cached address is therefore kept with the
+// unique id of the context it was looked up in (ids are never reused within
+// a process), and looked up again when the current context differs.
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;  // 0: none cached
+    void *ptr = nullptr;
+};
 std::mutex g_scratch_mu;
-void *g_scratch_addr[64] = {nullptr};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <class Fn>
+Fn driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the current context; 0 if none is current or it cannot be
+// read.
+unsigned long long current_ctx_id() {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace
 
-// Device address of g_decode_scratch on the current device.  In host code
+// Device address of g_decode_scratch in the current context.  In host code
 // the symbol names a host-side stand-in, not device memory, so the address
-// is asked for once per device, with that device current, and cached.
+// is asked for with the device current, once per context, and cached.
 int decode_static_scratch(void **ptr, size_t *bytes) {
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return record_message(FA_ERR_ARCH, "device ordinal out of range");
+    if (dev < 0 || dev >= kMaxDevices)
+        return record_message(FA_ERR_ARCH, "device ordinal out of range");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    unsigned long long id = current_ctx_id();
+    ScratchAddr &e = g_scratch_addr[dev];
+    if (id == 0 || e.ctx_id != id) {
+        // the lookup also makes the runtime's context current if none was
         void *p = nullptr;
         FA_CUDA_TRY(cudaGetSymbolAddress(&p, g_decode_scratch));
-        g_scratch_addr[dev] = p;
+        if (id == 0) id = current_ctx_id();
+        e.ptr = p;
+        e.ctx_id = id;  // 0 if the id cannot be read: looked up again next call
     }
-    *ptr = g_scratch_addr[dev];
+    *ptr = e.ptr;
     *bytes = kNoAllocScratchBytes;
     return FA_OK;
 }

@@ -513,31 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace f256
 
-static int sm_count_256(int dev) {
-    static int counts[64] = {0};
-    if (dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
-}
-
 template <bool CAUSAL>
 static int launch_256_t(const LaunchArgs &a) {
     auto kern = f256::fa_fwd256_kernel<CAUSAL>;
-    static int configured[64] = {0};
+    static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
-    if (!configured[dev]) {
-        FA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         f256::kSmemBytes));
-        configured[dev] = 1;
-    }
-    const int sms = sm_count_256(dev);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
+    const int rc = set_smem_once(configured, dev, kern, f256::kSmemBytes);
+    if (rc != FA_OK) return rc;
+    const int sms = device_sm_count(dev);
     if (sms <= 0) return record_message(FA_ERR_LAUNCH, "cannot query the SM count");
     f256::Params p;
     p.O = static_cast<__nv_bfloat16 *>(a.O);

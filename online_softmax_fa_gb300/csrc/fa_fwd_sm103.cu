@@ -635,35 +635,17 @@ __global__ void fa_wait_selftest_kernel(uint64_t limit_ns) {
     }
 }
 
-constexpr int kMaxDevices = 64;
-
-// SM count per device, queried once.
-static int sm_count(int dev) {
-    static int counts[kMaxDevices] = {0};
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
-}
-
 template <int D, bool CAUSAL>
 static int launch_t(const LaunchArgs &a) {
     using C = Cfg<D>;
     auto kern = fa_fwd_kernel<D, CAUSAL>;
-    static int configured[kMaxDevices] = {0};  // attribute set once per device
+    static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
     FA_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_ARCH;
-    if (!configured[dev]) {
-        FA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes));
-        configured[dev] = 1;
-    }
-    const int sms = sm_count(dev);
+    const int rc = set_smem_once(configured, dev, kern, C::kSmemBytes);
+    if (rc != FA_OK) return rc;
+    const int sms = device_sm_count(dev);
     if (sms <= 0) return record_message(FA_ERR_LAUNCH, "cannot query the SM count");
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(a.O);

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/fa.h"
@@ -78,6 +79,23 @@ int record_message(int status, const char *what);
         if (fa_e_ != cudaSuccess) return ::fa::record_cuda_error(fa_e_, #call); \
     } while (0)
 int read_and_clear_status(cudaStream_t stream, int *status);
+
+// Per-device facts kept for the life of the process, for device ordinals
+// 0 .. kMaxDevices - 1.  Several host threads may fill an entry at the same
+// time: they store the same value, and the entries are atomics, so the
+// first launch on a device needs no lock.
+constexpr int kMaxDevices = 64;
+// SM count of device `dev` (queried once), or 0 if the query fails.
+int device_sm_count(int dev);
+// Sets `kern`'s dynamic shared-memory limit to `bytes` the first time it is
+// launched on device `dev` (`flags`: one per device, zero-initialised).
+template <class Kern>
+int set_smem_once(std::atomic<int> *flags, int dev, Kern kern, int bytes) {
+    if (flags[dev].load(std::memory_order_acquire)) return FA_OK;
+    FA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    flags[dev].store(1, std::memory_order_release);
+    return FA_OK;
+}
 int launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fa

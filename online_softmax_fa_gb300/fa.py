@@ -48,6 +48,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_fwd_host_workspace_bytes.restype = S
     lib.fa_fwd_host.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, F, P]
     lib.fa_fwd_host.restype = I
+    lib.fa_fwd_host_gqa_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.fa_fwd_host_gqa_workspace_bytes.restype = S
+    lib.fa_fwd_host_gqa.argtypes = [P, P, P, P, P, P, S, I, I, I, I, I, I, F, P]
+    lib.fa_fwd_host_gqa.restype = I
     lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.fa_bwd_workspace_bytes.restype = S
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, S, I, I, I, I, I, F, P]
@@ -169,6 +173,28 @@ def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, workspace,
         B, H, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_host")
+
+
+def fa_fwd_host_gqa_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_host_gqa_workspace_bytes(B, H, H_kv, N, d))
+
+
+def fa_fwd_host_gqa(q_host, k_host, v_host, o_host, lse_host, workspace,
+                    causal: bool = False, scale: float | None = None, stream=None):
+    """fa_fwd_host for grouped-query attention: q_host, o_host [B, H, N, d];
+    k_host, v_host [B, H_kv, N, d] with H_kv dividing H; lse_host [B, H, N].
+    ``workspace``: CUDA uint8 tensor of at least
+    fa_fwd_host_gqa_workspace_bytes bytes.  Asynchronous, as fa_fwd_host."""
+    B, H, N, d = (int(x) for x in q_host.shape)
+    H_kv = int(k_host.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load_library().fa_fwd_host_gqa(
+        q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+        lse_host.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        B, H, H_kv, N, d, 1 if causal else 0, float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host_gqa")
 
 
 def fa_bwd(q, k, v, o, lse, do, dq=None, dk=None, dv=None, workspace=None,

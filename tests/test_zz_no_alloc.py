@@ -2,9 +2,10 @@
 
 The entry point keeps its split states in a library-owned area instead of a
 caller workspace.  These tests call it through the C ABI and check its
-output against fa_decode (the caller-workspace entry point) within the
-tolerances the other tests use, on two calls in a row with different inputs
-(so a second call cannot pass on what the first one left behind).  The file
+output against the fp64 oracle and against fa_decode (the caller-workspace
+entry point) within the tolerances the other tests use, on two calls in a
+row with different inputs (so a second call cannot pass on what the first
+one left behind).  The file
 sorts last so that a run stopping at the first failure has already run
 every other test; it also passes on its own in a fresh process.
 """
@@ -16,7 +17,7 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-O_MAX, LSE_MAX = 2e-2, 1e-3
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
 
 
 @pytest.fixture(scope="module")
@@ -52,15 +53,22 @@ def _noalloc(lib, q, k, v, scale):
 
 
 @pytest.mark.parametrize("B,H,H_kv,N,d", [(4, 8, 2, 3000, 128), (2, 16, 16, 1000, 64)])
-def test_noalloc_matches_workspace_decode_twice(lib, B, H, H_kv, N, d):
+def test_noalloc_matches_oracle_and_workspace_decode_twice(lib, B, H, H_kv, N, d):
+    import oracle
     from online_softmax_fa_gb300 import fa
+    from online_softmax_fa_gb300.inputs import make_decode
     scale = float(np.float32(1 / np.sqrt(d)))
     for seed in (101, 202):  # two calls in a row, different inputs
+        q_h, k_h, v_h = make_decode(B, H, H_kv, N, d, seed)
         q, k, v = _inputs(seed, B, H, H_kv, N, d)
         o_na, l_na = _noalloc(lib, q, k, v, scale)
         o_ws, l_ws = fa.fa_decode(q, k, v, scale=scale)
         torch.cuda.synchronize()
         assert fa.fa_device_error() == 0
+        O_ref, L_ref = oracle.attention_decode(q_h.unsqueeze(2), k_h, v_h, scale=scale)
+        eo = np.abs(o_na.float().cpu().numpy() - O_ref[:, :, 0])
+        el = np.abs(l_na.cpu().numpy() - L_ref[:, :, 0])
+        assert eo.max() <= O_MAX and eo.mean() <= O_MEAN and el.max() <= LSE_MAX
         assert (o_na.float() - o_ws.float()).abs().max().item() <= O_MAX
         assert (l_na - l_ws).abs().max().item() <= LSE_MAX
         assert torch.isfinite(l_na).all()
