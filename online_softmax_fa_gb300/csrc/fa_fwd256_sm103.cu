@@ -13,8 +13,12 @@
 // warps turn S(j) into P(j), and O += P(j) V_j follows.  Per key tile the
 // tensor pipe has 2 x 1024 cycles of work and the softmax of a 128 x 128
 // tile takes less, so the pipe, not the softmax, sets the pace.
-//   * warp 5 (TMA): per item the query block (4 boxes of 64 columns), then
-//     K tiles in halves of 128 columns (d) through a 3-stage ring.
+//   * warp 5 (TMA and schedule): per item the query block (4 boxes of 64
+//     columns), then K tiles in halves of 128 columns (d) through a 3-stage
+//     ring; it claims the next item (cluster launch control: the grid has a
+//     CTA per item, and a running CTA cancels the launch of the next one and
+//     does its item) and passes it on through a two-slot ring, exactly as
+//     in the d <= 128 kernel, with the same order of items.
 //   * warp 6 (TMA): V tiles in halves of 64 keys through a 2-stage ring.
 //   * warp 4 (MMA): S(j) as 16 MMAs of M128 x N128 x K16 (K over d), P(j)V_j
 //     as 8 MMAs of M128 x N256 x K16 (K over keys) with P read from TMEM.
@@ -56,20 +60,26 @@ constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStagesK * kKStage;
 constexpr int kOffBar = kOffV + kStagesV * kVStage;
 // q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2],
-// p_full, o_ready, o_full, o_empty, mma_done
-constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 5;
-constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+// p_full, o_ready, o_full, o_empty, mma_done, sched_full[2], sched_empty[2],
+// claim; then (16-byte aligned) the tmem slot, the abort flag, the two item
+// slots and the 16-byte claim answer
+constexpr int kNumBars = 2 + 2 * kStagesK + 2 * kStagesV + 2 + 5 + 5;
+constexpr int kOffMisc = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
+constexpr int kSmemBytes = kOffMisc + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmO = 0, kTmS = 256;  // S buffer b at kTmS + 128 b
 constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, kD, true);
 constexpr float kStaleMax = 8.0f;
+// Causal: the next item is claimed this many key tiles before the end of the
+// current item's K loads (see the d <= 128 kernel); without a mask at the
+// start of an item.
+constexpr int kClaimLead = 3;
 
 enum : int {
     kSiteQ = 0x41, kSiteK, kSiteV, kSiteP, kSiteS, kSiteOReady, kSiteOFull, kSiteOEmpty,
-    kSiteQEmpty, kSiteKEmpty, kSiteVEmpty
+    kSiteQEmpty, kSiteKEmpty, kSiteVEmpty, kSiteSchedFull, kSiteSchedEmpty, kSiteClaim
 };
 
 struct Params {
@@ -78,7 +88,9 @@ struct Params {
     int N, BH, H, group;
     int n_qblocks;  // ceil(N / 128)
     int n_ktiles;   // ceil(N / 128)
-    int n_items;    // BH x n_qblocks
+    int n_items;    // BH x n_qblocks = the grid
+    int head_group;   // causal order: heads per group
+    int first_group;  // heads in the first (partial) group
     float scale_log2;
     uint64_t limit_ns;
 };
@@ -86,9 +98,11 @@ struct Params {
 struct View {
     uint8_t *q, *k, *v;
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full,
-        *o_ready, *o_full, *o_empty, *mma_done;
+        *o_ready, *o_full, *o_empty, *mma_done, *sched_full, *sched_empty, *claim;
     uint32_t *tmem_slot;
     volatile int *abort_flag;
+    volatile int *sched_item;  // [2]: work item, or -1 = no more work
+    void *claim_resp;          // 16 bytes, 16-byte aligned
 };
 
 __device__ __forceinline__ View view() {
@@ -112,8 +126,13 @@ __device__ __forceinline__ View view() {
     v.o_full = v.o_ready + 1;
     v.o_empty = v.o_full + 1;
     v.mma_done = v.o_empty + 1;
+    v.sched_full = v.mma_done + 1;
+    v.sched_empty = v.sched_full + 2;
+    v.claim = v.sched_empty + 2;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    v.sched_item = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    v.claim_resp = smem + kOffMisc + 16;
     return v;
 }
 
@@ -121,15 +140,34 @@ struct Work {
     int bh, kvh, qb, n;  // n: key tiles this query block needs
 };
 
+// Work item x (the grid's CTA index, in priority order) -> (head, query
+// block), as in the d <= 128 kernel: causal, heads in groups (the partial
+// group first) and inside a group the heaviest query block first with the
+// group's heads interleaved; otherwise head-major.
 template <bool CAUSAL>
 __device__ __forceinline__ Work work_of(const Params &p, int x) {
     Work w;
-    if (CAUSAL) {  // heaviest (last) query blocks first, heads interleaved
-        w.qb = p.n_qblocks - 1 - x / p.BH;
-        w.bh = x % p.BH;
+    if (CAUSAL) {
+        const int nq = p.n_qblocks;
+        const int first = p.first_group * nq;  // items of the first group
+        int h0, gs, in;
+        if (x < first) {
+            h0 = 0;
+            gs = p.first_group;
+            in = x;
+        } else {
+            const int y = x - first, per = p.head_group * nq;
+            const int g = y / per;
+            h0 = p.first_group + g * p.head_group;
+            gs = p.head_group;
+            in = y - g * per;
+        }
+        const int level = in / gs;
+        w.qb = nq - 1 - level;
+        w.bh = h0 + (in - level * gs);
     } else {
         w.bh = x / p.n_qblocks;
-        w.qb = x % p.n_qblocks;
+        w.qb = x - w.bh * p.n_qblocks;
     }
     const int b = w.bh / p.H, h = w.bh - b * p.H;
     w.kvh = b * (p.H / p.group) + h / p.group;
@@ -138,11 +176,19 @@ __device__ __forceinline__ Work work_of(const Params &p, int x) {
     return w;
 }
 
-// Snake order over the CTAs, as in the d <= 128 kernel.
-__device__ __forceinline__ int item_of(int r, int n_items) {
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int x = r * G + ((r & 1) ? (G - 1 - c) : c);
-    return x < n_items ? x : -1;
+// The r-th work item of this CTA as the Q/K load warp published it (-1: no
+// more work).  Called by every thread of a consumer warp; one lane then
+// frees the slot.
+__device__ __forceinline__ bool next_item(const View &v, const WaitCtl &ctl, int r, int lane,
+                                          int &x) {
+    const int slot = r & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(&v.sched_full[slot], (r >> 1) & 1, ctl,
+                                           kSiteSchedFull)))
+        return false;
+    x = v.sched_item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&v.sched_empty[slot]);
+    return true;
 }
 
 // ---------------------------------------------------------------- producers
@@ -152,12 +198,23 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
     if (lane != 0) return;
     const View v = view();
     const WaitCtl ctl{v.abort_flag, &g_fa_status_256, p.limit_ns};
-    const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     int u = 0;      // K halves issued, across items
     int items = 0;  // query blocks issued
+    // claims: 2 x (claims answered so far) + (1 if one is on its way); -1
+    // once a claim has failed (no further claim may be made)
+    int claims = 0;
     bool ok = true;
-    for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
+    int x = static_cast<int>(blockIdx.x);  // this CTA's own item first
+    for (int r = 0;; ++r) {
+        // publish item x (or the end of the work); slot r & 1 last held
+        // item r - 2
+        const int slot = r & 1;
+        if (r >= 2) {
+            ok = mbar_wait(&v.sched_empty[slot], ((r >> 1) & 1) ^ 1, ctl, kSiteSchedEmpty);
+            if (!ok) break;
+        }
+        v.sched_item[slot] = x;
+        mbar_arrive(&v.sched_full[slot]);
         if (x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         if (r > 0) {  // the previous item's last S has read Q
@@ -165,10 +222,20 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
             if (!ok) break;
         }
         mbar_arrive_expect_tx(v.q_full, kQBytes);
-        for (int c = 0; c < 4; ++c)
-            tma_load_3d(v.q + c * kBox, tmQ, v.q_full, 64 * c, w.qb * kBlockM, w.bh, pol_q);
+        {
+            const uint64_t pol_q = l2_policy_evict_first();
+            for (int c = 0; c < 4; ++c)
+                tma_load_3d(v.q + c * kBox, tmQ, v.q_full, 64 * c, w.qb * kBlockM, w.bh, pol_q);
+        }
         ++items;
+        const int claim_at = CAUSAL ? max(0, w.n - kClaimLead) : 0;
         for (int j = 0; j < w.n && ok; ++j) {
+            if (j == claim_at && claims >= 0) {  // ask for the next item
+                mbar_arrive_expect_tx(v.claim, 16);
+                clc_try_cancel(v.claim_resp, v.claim);
+                claims |= 1;
+            }
+            const uint64_t pol_kv = l2_policy_evict_last();
             for (int h = 0; h < 2; ++h) {  // d columns [128h, 128h + 128)
                 const int s = u % kStagesK;
                 if (u >= kStagesK)
@@ -181,40 +248,60 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
                 ++u;
             }
         }
+        if (!ok) break;
+        // the next item: the cancelled CTA's, if the claim succeeded
+        x = -1;
+        if (claims > 0 && (claims & 1)) {
+            ok = mbar_wait(v.claim, (claims >> 1) & 1, ctl, kSiteClaim);
+            if (!ok) break;
+            claims += 1;  // answered: clear the pending bit, count it
+            x = clc_cancelled_x(v.claim_resp);
+            if (x < 0) claims = -1;
+        }
     }
+    // drain the query block, the K stages and a claim answer in flight
     if (items > 0) mbar_wait_drain(v.q_full, (items - 1) & 1, p.limit_ns);
     for (int t = max(0, u - kStagesK); t < u; ++t)
         mbar_wait_drain(&v.k_full[t % kStagesK], (t / kStagesK) & 1, p.limit_ns);
+    if (claims > 0 && (claims & 1)) mbar_wait_drain(v.claim, (claims >> 1) & 1, p.limit_ns);
 }
 
 template <bool CAUSAL>
 __device__ __forceinline__ void role_load_v(const CUtensorMap *tmV64, const Params &p, int lane) {
-    if (lane != 0) return;
+    // the whole warp walks the items (the item ring is read warp-wide);
+    // lane 0 waits for ring stages and issues the loads
     const View v = view();
     const WaitCtl ctl{v.abort_flag, &g_fa_status_256, p.limit_ns};
-    const uint64_t pol_kv = l2_policy_evict_last();
-    int u = 0;  // V halves issued, across items
+    int u = 0;  // V halves issued, across items (lane 0)
     bool ok = true;
     for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
-        if (x < 0) break;
+        int x;
+        ok = next_item(v, ctl, r, lane, x);
+        if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
-        for (int j = 0; j < w.n && ok; ++j) {
-            for (int h = 0; h < 2; ++h) {  // keys [64h, 64h + 64) of tile j
-                const int s = u % kStagesV;
-                if (u >= kStagesV)
-                    ok = mbar_wait(&v.v_empty[s], ((u / kStagesV) & 1) ^ 1, ctl, kSiteVEmpty);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&v.v_full[s], kVStage);
-                for (int c = 0; c < 4; ++c)
-                    tma_load_3d(v.v + s * kVStage + c * kVBox, tmV64, &v.v_full[s], 64 * c,
-                                j * kBlockN + 64 * h, w.kvh, pol_kv);
-                ++u;
+        if (lane == 0) {
+            const uint64_t pol_kv = l2_policy_evict_last();
+            for (int j = 0; j < w.n && ok; ++j) {
+                for (int h = 0; h < 2; ++h) {  // keys [64h, 64h + 64) of tile j
+                    const int s = u % kStagesV;
+                    if (u >= kStagesV)
+                        ok = mbar_wait(&v.v_empty[s], ((u / kStagesV) & 1) ^ 1, ctl,
+                                       kSiteVEmpty);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&v.v_full[s], kVStage);
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(v.v + s * kVStage + c * kVBox, tmV64, &v.v_full[s],
+                                    64 * c, j * kBlockN + 64 * h, w.kvh, pol_kv);
+                    ++u;
+                }
             }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
-    for (int t = max(0, u - kStagesV); t < u; ++t)
-        mbar_wait_drain(&v.v_full[t % kStagesV], (t / kStagesV) & 1, p.limit_ns);
+    if (lane == 0)
+        for (int t = max(0, u - kStagesV); t < u; ++t)
+            mbar_wait_drain(&v.v_full[t % kStagesV], (t / kStagesV) & 1, p.limit_ns);
+    __syncwarp();
 }
 
 // -------------------------------------------------------------- MMA issuer
@@ -252,10 +339,12 @@ __device__ __forceinline__ void role_mma(const Params &p) {
         }
         return true;
     };
+    const int lane = static_cast<int>(threadIdx.x & 31);
     bool ok = true;
     for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
-        if (x < 0) break;
+        int x;
+        ok = next_item(v, ctl, r, lane, x);
+        if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         ok = wait(v.q_full, r & 1, kSiteQ);
         if (!ok) break;
@@ -332,8 +421,9 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
     int t = 0;  // key tiles consumed, across items
     bool ok = true;
     for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
-        if (x < 0) break;
+        int x;
+        ok = next_item(v, ctl, r, lane, x);
+        if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int qrow = w.qb * kBlockM + row;
         // reference max m (base 2, scale folded in) and running sum l; the
@@ -478,6 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(v.o_full, 1);
             mbar_init(v.o_empty, 4);
             mbar_init(v.mma_done, 1);
+            for (int k = 0; k < 2; ++k) {
+                mbar_init(&v.sched_full[k], 1);
+                mbar_init(&v.sched_empty[k], 6);  // V load, MMA and 4 softmax warps
+            }
+            mbar_init(v.claim, 1);
             *v.abort_flag = 0;
             fence_mbarrier_init();
         }
@@ -538,8 +633,17 @@ static int launch_256_t(const LaunchArgs &a) {
     p.n_items = static_cast<int>(items);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
-    const int grid = static_cast<int>(items < sms ? items : sms);
-    kern<<<grid, f256::kThreads, f256::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV64, p);
+    // causal head groups of about two waves of their heaviest items, whole
+    // K/V groups, at most all heads (as in the d <= 128 kernel)
+    long long hg = (2LL * sms + p.n_qblocks) / (p.n_qblocks + 1);
+    hg = (hg + p.group - 1) / p.group * p.group;
+    if (hg > a.BH) hg = a.BH;
+    if (hg < 1) hg = 1;
+    p.head_group = static_cast<int>(hg);
+    p.first_group = a.BH % p.head_group == 0 ? p.head_group : a.BH % p.head_group;
+    // one CTA per work item; the CTAs that run take over the others' items
+    kern<<<p.n_items, f256::kThreads, f256::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV64,
+                                                                     p);
     FA_CUDA_TRY(cudaGetLastError());
     return FA_OK;
 }

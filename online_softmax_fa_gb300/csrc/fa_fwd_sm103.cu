@@ -12,16 +12,25 @@
 //
 // GB300 mapping.  A work item is one (b, h, 256-row query block): query
 // blocks are the outer loop and own their output ("Fix 3"), and the grid
-// covers batch x heads x query blocks ("Fix 4").  The kernel is persistent:
-// one CTA per SM walks a static schedule of work items, heaviest first
-// (causal blocks differ in cost), assigned in a snake order over the CTAs
-// so the per-CTA totals balance ("the assignment of blocks to SMs must
-// account for the imbalance").  Consecutive items overlap: the next item's
-// query block loads and its first S tiles are computed while the softmax
-// warps write the previous item's output.
-//   * warp 9 (TMA): per item, the query block once, then 128-key K and V
-//     tiles through separate multi-stage shared-memory rings that run on
-//     across items.
+// covers batch x heads x query blocks ("Fix 4").  The grid has one CTA per
+// work item, in priority order, but only one CTA fits on an SM and the CTAs
+// that run steal the rest: before a CTA runs out of work it asks the
+// hardware scheduler (cluster launch control) to cancel the launch of the
+// next CTA of the grid and does that CTA's item itself.  So each SM keeps
+// its CTA (and its warm pipeline) while the items are handed out greedily
+// in grid order, which balances the causal costs ("the assignment of blocks
+// to SMs must account for the imbalance").  Causal order: heads in groups
+// (the partial group first), inside a group the heaviest query block first
+// with the group's heads interleaved; a group's K/V stays in L2 while its
+// items run, and every group holds enough heavy items that its last ones
+// start early.  Consecutive items of a CTA overlap: the next item's query
+// block loads and its first S tiles are computed while the softmax warps
+// write the previous item's output.
+//   * warp 9 (TMA and schedule): per item, the query block once, then
+//     128-key K and V tiles through separate multi-stage shared-memory rings
+//     that run on across items; a few tiles before an item's loads end it
+//     claims the next item and passes it to the other warps through a
+//     two-slot ring in shared memory.
 //   * warp 8 (MMA): tcgen05 MMAs issued by one elected lane of a converged
 //     warp.  The query block is two 128-row sub-tiles; S_k = Q_k K_j^T lands
 //     in TMEM (fp32), and O_k += P_k V_j reads P_k from TMEM (bf16, written
@@ -73,11 +82,18 @@ constexpr uint32_t kTmemCols = 512;
 // The running reference max moves only when a row's max exceeds it by more
 // than this many base-2 units (factor 256); probabilities then stay <= 256.
 constexpr float kStaleMax = 8.0f;
+// Causal: the next work item is claimed this many key tiles before the end
+// of the current item's loads: late enough that the CTA is nearly free
+// (greedy hand-out in grid order over items of unequal cost), early enough
+// that the answer is back before the next query block is due.  Items of
+// equal cost (no mask) are claimed as an item's loads begin.
+constexpr int kClaimLead = 3;
 
 // wait sites recorded in the status word on a timeout
 enum : int {
     kSiteQ = 1, kSiteKFull, kSiteVFull, kSitePFull, kSiteKEmpty, kSiteVEmpty,
-    kSiteSFull, kSiteOFull, kSiteQEmpty, kSiteOEmpty
+    kSiteSFull, kSiteOFull, kSiteQEmpty, kSiteOEmpty, kSiteSchedFull, kSiteSchedEmpty,
+    kSiteClaim
 };
 
 template <int D>
@@ -91,11 +107,12 @@ struct Cfg {
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
     // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S],
-    // v_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], mma_done;
-    // then the tmem slot and the abort flag
-    static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    // v_empty[S], s_full[2], p_full[2], o_full[2], o_empty[2], mma_done,
+    // sched_full[2], sched_empty[2], claim; then (16-byte aligned) the tmem
+    // slot, the abort flag, the two item slots and the 16-byte claim answer
+    static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1 + 2 + 2 + 1;
+    static constexpr int kOffMisc = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
+    static constexpr int kSmemBytes = kOffMisc + 32 + 1024;  // + alignment slack
     static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kSubM, kBlockN, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kSubM, D, true);
@@ -135,7 +152,9 @@ struct Params {
     int group;      // query heads per K/V head (grouped-query attention; 1 = MHA)
     int n_qblocks;  // ceil(N / 256)
     int n_ktiles;   // ceil(N / 128)
-    int n_items;    // BH x n_qblocks
+    int n_items;    // BH x n_qblocks = the grid
+    int head_group;   // causal order: heads per group
+    int first_group;  // heads in the first (partial) group
     float scale_log2;  // scale * log2(e)
     uint64_t limit_ns;
     int o_align32;     // O is 32-byte aligned: the epilogue stores 32 bytes at a time
@@ -148,8 +167,11 @@ struct SmemView {
     uint8_t *q, *k, *v;
     uint64_t *q_full, *q_empty, *k_full, *k_empty, *v_full, *v_empty;
     uint64_t *s_full, *p_full, *o_full, *o_empty, *mma_done;
+    uint64_t *sched_full, *sched_empty, *claim;
     uint32_t *tmem_slot;
     volatile int *abort_flag;
+    volatile int *sched_item;  // [2]: work item, or -1 = no more work
+    void *claim_resp;          // 16 bytes, 16-byte aligned
 };
 
 template <int D>
@@ -175,15 +197,22 @@ __device__ __forceinline__ SmemView<D> smem_view() {
     v.o_full = v.p_full + 2;
     v.o_empty = v.o_full + 2;
     v.mma_done = v.o_empty + 2;
+    v.sched_full = v.mma_done + 1;
+    v.sched_empty = v.sched_full + 2;
+    v.claim = v.sched_empty + 2;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    v.sched_item = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
+    v.claim_resp = smem + C::kOffMisc + 16;
     return v;
 }
 
 // ------------------------------------------------------------- schedule
-// Work items in cost order.  Causal: heaviest query block first (block qb
-// needs 2*qb + 2 key tiles), heads interleaved; otherwise head-major (equal
-// cost, and consecutive items share K/V in L2).
+// Work item x (the grid's CTA index, in priority order) -> (head, query
+// block).  Causal: heads in groups of head_group, the partial group
+// (first_group heads) first; inside a group the heaviest query block first
+// (block qb needs 2*qb + 2 key tiles), the group's heads interleaved.
+// Otherwise head-major (equal costs; consecutive items share K/V in L2).
 struct Work {
     int bh, kvh, qb, n_sub0, n_sub1;  // kvh: K/V head row; n_sub1 >= n_sub0
 };
@@ -192,15 +221,30 @@ template <bool CAUSAL>
 __device__ __forceinline__ Work work_of(const Params &p, int x) {
     Work w;
     if (CAUSAL) {
-        w.qb = p.n_qblocks - 1 - x / p.BH;
-        w.bh = x % p.BH;
+        const int nq = p.n_qblocks;
+        const int first = p.first_group * nq;  // items of the first group
+        int h0, gs, in;
+        if (x < first) {
+            h0 = 0;
+            gs = p.first_group;
+            in = x;
+        } else {
+            const int y = x - first, per = p.head_group * nq;
+            const int g = y / per;
+            h0 = p.first_group + g * p.head_group;
+            gs = p.head_group;
+            in = y - g * per;
+        }
+        const int level = in / gs;
+        w.qb = nq - 1 - level;
+        w.bh = h0 + (in - level * gs);
     } else {
         w.bh = x / p.n_qblocks;
-        w.qb = x % p.n_qblocks;
+        w.qb = x - w.bh * p.n_qblocks;
     }
     // grouped-query attention: query head h of batch b reads K/V head
     // h / group of that batch (consecutive query heads share one K/V head,
-    // and the schedule keeps them adjacent, so they share it in L2)
+    // and the order keeps them adjacent, so they share it in L2)
     const int b = w.bh / p.H, h = w.bh - b * p.H;
     w.kvh = b * (p.H / p.group) + h / p.group;
     const int T = p.n_ktiles, N = p.N;
@@ -210,14 +254,20 @@ __device__ __forceinline__ Work work_of(const Params &p, int x) {
     return w;
 }
 
-// The r-th work item of this CTA: rows of gridDim.x items, walked left to
-// right on even rows and right to left on odd rows (a snake), so that a CTA
-// taking a heavy item from one row takes a light one from the next.
-// Returns -1 past the end.
-__device__ __forceinline__ int item_of(int r, int n_items) {
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int x = r * G + ((r & 1) ? (G - 1 - c) : c);
-    return x < n_items ? x : -1;
+// The r-th work item of this CTA as the producer published it (-1: no more
+// work).  Called by every thread of a consumer warp; one lane then frees the
+// slot.
+template <int D>
+__device__ __forceinline__ bool next_item(const SmemView<D> &v, const WaitCtl &ctl, int r,
+                                          int lane, int &x) {
+    const int slot = r & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(&v.sched_full[slot], (r >> 1) & 1, ctl,
+                                           kSiteSchedFull)))
+        return false;
+    x = v.sched_item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&v.sched_empty[slot]);
+    return true;
 }
 
 // ================================ TMA producer ================================
@@ -229,13 +279,23 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
     if (lane != 0) return;
     const SmemView<D> v = smem_view<D>();
     const WaitCtl ctl{v.abort_flag, &g_fa_status, p.limit_ns};
-    const uint64_t pol_q = l2_policy_evict_first();
-    const uint64_t pol_kv = l2_policy_evict_last();
     int g = 0;       // K/V tiles issued so far, across items
     int items = 0;   // query blocks issued so far
+    // claims: 2 x (claims answered so far) + (1 if one is on its way); -1
+    // once a claim has failed (no further claim may be made)
+    int claims = 0;
     bool ok = true;
-    for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
+    int x = static_cast<int>(blockIdx.x);  // this CTA's own item first
+    for (int r = 0;; ++r) {
+        // publish item x (or the end of the work) to the MMA and softmax
+        // warps; slot r & 1 last held item r - 2
+        const int slot = r & 1;
+        if (r >= 2) {
+            ok = mbar_wait(&v.sched_empty[slot], ((r >> 1) & 1) ^ 1, ctl, kSiteSchedEmpty);
+            if (!ok) break;
+        }
+        v.sched_item[slot] = x;
+        mbar_arrive(&v.sched_full[slot]);
         if (x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         if (r > 0) {  // the previous item's last S MMA has read Q
@@ -243,12 +303,22 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
             if (!ok) break;
         }
         mbar_arrive_expect_tx(v.q_full, C::kQBytes);
-        for (int k = 0; k < 2; ++k)
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(v.q + (k * C::kChunks + c) * kBoxBytes, tmQ, v.q_full, 64 * c,
-                            w.qb * kBlockM + k * kSubM, w.bh, pol_q);
+        {
+            const uint64_t pol_q = l2_policy_evict_first();
+            for (int k = 0; k < 2; ++k)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(v.q + (k * C::kChunks + c) * kBoxBytes, tmQ, v.q_full, 64 * c,
+                                w.qb * kBlockM + k * kSubM, w.bh, pol_q);
+        }
         ++items;
+        const int claim_at = CAUSAL ? max(0, w.n_sub1 - kClaimLead) : 0;
         for (int j = 0; j < w.n_sub1; ++j) {
+            if (j == claim_at && claims >= 0) {  // ask for the next item
+                mbar_arrive_expect_tx(v.claim, 16);
+                clc_try_cancel(v.claim_resp, v.claim);
+                claims |= 1;
+            }
+            const uint64_t pol_kv = l2_policy_evict_last();
             const int t = g + j, s = t % C::kStages;
             const uint32_t ph = (t / C::kStages) & 1;
             if (t >= C::kStages) ok = mbar_wait(&v.k_empty[s], ph ^ 1, ctl, kSiteKEmpty);
@@ -270,17 +340,30 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
                 tma_load_3d(v.v + s * C::kTileBytes + c * kBoxBytes, tmV, &v.v_full[s], 64 * c,
                             j * kBlockN, w.kvh, pol_kv);
         }
-        if (ok) g += w.n_sub1;
+        if (!ok) break;
+        g += w.n_sub1;
+        // the next item: the cancelled CTA's, if the claim succeeded; after
+        // a failed claim none is made again
+        x = -1;
+        if (claims > 0 && (claims & 1)) {
+            ok = mbar_wait(v.claim, (claims >> 1) & 1, ctl, kSiteClaim);
+            if (!ok) break;
+            claims += 1;  // answered: clear the pending bit, count it
+            x = clc_cancelled_x(v.claim_resp);
+            if (x < 0) claims = -1;
+        }
     }
-    // Drain: every load issued must land before the CTA exits.  The last
-    // query block, and the last load of each ring stage (after an abort V
-    // may lag K by one tile; a wait on a phase that never started times out
-    // after the limit, a wait on one that completed returns at once).
+    // Drain: every asynchronous write into shared memory lands before the
+    // CTA exits.  The last query block, the last load of each ring stage
+    // (after an abort V may lag K by one tile; a wait on a phase that never
+    // started times out after the limit, a wait on one that completed
+    // returns at once), and a claim answer still on its way.
     if (items > 0) mbar_wait_drain(v.q_full, (items - 1) & 1, p.limit_ns);
     for (int t = max(0, g - C::kStages); t < g; ++t) {
         mbar_wait_drain(&v.k_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
         mbar_wait_drain(&v.v_full[t % C::kStages], (t / C::kStages) & 1, p.limit_ns);
     }
+    if (claims > 0 && (claims & 1)) mbar_wait_drain(v.claim, (claims >> 1) & 1, p.limit_ns);
 }
 
 // ================================= MMA issuer =================================
@@ -303,12 +386,14 @@ __device__ __forceinline__ void role_mma(const Params &p) {
     const auto wait = [&](uint64_t *bar, uint32_t parity, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
     };
+    const int lane = static_cast<int>(threadIdx.x & 31);
     int g = 0;             // K/V tiles consumed, across items
     int pc0 = 0, pc1 = 0;  // P tiles consumed per sub-tile, across items
     bool ok = true;
     for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
-        if (x < 0) break;
+        int x;
+        ok = next_item(v, ctl, r, lane, x);
+        if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int n0 = w.n_sub0, n1 = w.n_sub1;
         ok = wait(v.q_full, r & 1, kSiteQ);
@@ -421,8 +506,9 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
     int sc = 0;  // S tiles consumed, across items
     bool ok = true;
     for (int r = 0; ok; ++r) {
-        const int x = item_of(r, p.n_items);
-        if (x < 0) break;
+        int x;
+        ok = next_item(v, ctl, r, lane, x);
+        if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int sub_start = w.qb * kBlockM + k * kSubM;
         const int qrow = sub_start + row;
@@ -579,6 +665,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&v.o_empty[k], 4);
             }
             mbar_init(v.mma_done, 1);
+            for (int k = 0; k < 2; ++k) {
+                mbar_init(&v.sched_full[k], 1);
+                mbar_init(&v.sched_empty[k], 9);  // the MMA warp and 8 softmax warps
+            }
+            mbar_init(v.claim, 1);
             *v.abort_flag = 0;
             fence_mbarrier_init();
         }
@@ -662,9 +753,18 @@ static int launch_t(const LaunchArgs &a) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
     p.o_align32 = (reinterpret_cast<uintptr_t>(a.O) & 31u) == 0 ? 1 : 0;
-    // one persistent CTA per SM (the shared-memory footprint allows one)
-    const int grid = static_cast<int>(items < sms ? items : sms);
-    kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, p);
+    // Causal head groups: each group holds about two waves of its heaviest
+    // items (a head brings n_qblocks items, the heaviest twice the average),
+    // whole K/V groups of grouped-query heads, at most all heads.
+    long long hg = (2LL * sms + p.n_qblocks) / (p.n_qblocks + 1);
+    hg = (hg + p.group - 1) / p.group * p.group;
+    if (hg > a.BH) hg = a.BH;
+    if (hg < 1) hg = 1;
+    p.head_group = static_cast<int>(hg);
+    p.first_group = a.BH % p.head_group == 0 ? p.head_group : a.BH % p.head_group;
+    // one CTA per work item; one fits on an SM (shared memory), and the
+    // CTAs that run take over the others' items (cluster launch control)
+    kern<<<p.n_items, kThreads, C::kSmemBytes, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, p);
     FA_CUDA_TRY(cudaGetLastError());
     return FA_OK;
 }

@@ -137,6 +137,37 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// ------------------------------------------------- cluster launch control
+// Work stealing with the hardware scheduler: a running CTA asks it to cancel
+// the launch of a CTA of the same grid that has not started yet and, if it
+// succeeds, does that CTA's work itself.  The 16-byte response lands in
+// shared memory (16-byte aligned) and completes 16 bytes on `bar` (arm the
+// barrier with mbar_arrive_expect_tx(bar, 16)).  After a failed request has
+// been observed, no further request may be issued.
+__device__ __forceinline__ void clc_try_cancel(void *resp, uint64_t *bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+        " [%0], [%1];" ::"r"(smem_u32(resp)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Decodes a completed response: the x index of the cancelled CTA, or -1 if
+// nothing was cancelled (no CTA of the grid is left to launch).
+__device__ __forceinline__ int clc_cancelled_x(const void *resp) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(smem_u32(resp))
+        : "memory");
+    return ok ? static_cast<int>(x) : -1;
+}
+
 // --------------------------------------------------------------------- TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
