@@ -389,9 +389,187 @@ def run_ours(args, w, causal):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if ws == 1 and not args.no_secondary:
+        out["secondary"] = secondary_legs(dev, fa, peak, peak_kind)
     if ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, causal)
     print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------- secondary legs
+def time_device(step, n, warmup, steps, stream):
+    """Runs step(i) `warmup` times, then times `steps` calls with CUDA events
+    on `stream` (synchronised on both sides).  Returns (mean ms per call
+    over the whole timed region, per-call ms list)."""
+    import torch
+    for i in range(warmup):
+        step(i % n)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        step(i % n)
+        ends[i].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def secondary_legs(dev, fa, peak, peak_kind):
+    """The other rows of the hot path, measured in the same process after
+    the headline leg, a few steps each: the backward pass on the llama
+    workload, the grouped-query forward (device and host buffers), the
+    d = 256 forward, decoding against a K/V cache, the latency-bound small
+    workloads, and the oracle on the small workloads (one thread and all)."""
+    import torch
+    import oracle
+    from online_softmax_fa_gb300.inputs import make_grad
+    stream = torch.cuda.current_stream()
+    out = {}
+    status = []
+
+    def fwd_leg(name, steps, e2e_steps=0):
+        w = WORKLOADS[name]
+        causal = w.causal[-1]
+        q, k, v = make_workload(w)
+        gqa = w.kv_heads != w.H
+        f = fa.fa_fwd_gqa if gqa else fa.fa_fwd
+        sets = [(q.to(dev), k.to(dev), v.to(dev)) for _ in range(3)]
+        outs = [(torch.empty_like(sets[0][0]),
+                 torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev))
+                for _ in range(3)]
+
+        def step(i):
+            f(*sets[i], o=outs[i][0], lse=outs[i][1], causal=causal, scale=w.scale)
+        ms, per = time_device(step, 3, 5, steps, stream)
+        status.append(fa.fa_device_error())
+        tf = w.flops(causal) / (ms * 1e-3) / 1e12
+        leg = {"workload": workload_config(w, causal)["workload"], "value": tf,
+               "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+               "kernel_ms_median": statistics.median(per),
+               "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                            "frac": tf / peak, "peak_source": f"bf16_tflops of {peak_kind}"}}
+        del sets, outs
+        if e2e_steps:
+            host = fa.fa_fwd_host_gqa if gqa else fa.fa_fwd_host
+            wbytes = (fa.fa_fwd_host_gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d)
+                      if gqa else fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d))
+            wsp = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+            qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+            oh = torch.empty_like(q).pin_memory()
+            lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+            ms_h, _ = time_device(lambda i: host(qh, kh, vh, oh, lh, wsp, causal=causal,
+                                                 scale=w.scale), 1, 2, e2e_steps, stream)
+            status.append(fa.fa_device_error())
+            leg["e2e"] = {"value": w.flops(causal) / (ms_h * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "ms_per_step": ms_h, "steps": e2e_steps,
+                          "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                          "d2h_bytes_per_step": q.numel() * 2 + w.B * w.H * w.N * 4,
+                          "api": ("fa_fwd_host_gqa" if gqa else "fa_fwd_host")}
+        return leg
+
+    out["gqa_forward"] = fwd_leg("llama_gqa", 100, e2e_steps=10)
+    out["d256_forward"] = fwd_leg("d256", 100)
+
+    # backward on the llama workload (5 nominal N x N x d products)
+    w = WORKLOADS["llama"]
+    q, k, v = (t.to(dev) for t in make_workload(w))
+    do = make_grad(w.B, w.H, w.N, w.d, w.seed).to(dev)
+    o, lse = fa.fa_fwd(q, k, v, causal=True, scale=w.scale)
+    grads = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
+    wsb = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                      device=dev)
+
+    def bstep(i):
+        fa.fa_bwd(q, k, v, o, lse, do, *grads[i], workspace=wsb, causal=True, scale=w.scale)
+    ms, per = time_device(bstep, 2, 5, 100, stream)
+    status.append(fa.fa_device_error())
+    tf = 2.5 * w.flops(True) / (ms * 1e-3) / 1e12
+    out["backward"] = {"workload": "llama attention backward B1 H32 N8192 d128 causal",
+                       "metric": "TFLOP/s over 10*B*H*N^2*d, causal halved",
+                       "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "steps": 100,
+                       "kernel_ms_median": statistics.median(per), "launches_per_step": 3,
+                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                                    "frac": tf / peak,
+                                    "peak_source": f"bf16_tflops of {peak_kind}"}}
+    del q, k, v, do, o, lse, grads, wsb
+
+    # decoding: one new query row per head against an 8192-position cache
+    wd = DECODE_WORKLOADS["decode"]
+    qd, kd, vd = make_decode(wd.B, wd.H, wd.kv_heads, wd.N, wd.d, wd.seed)
+    need = fa.fa_decode_workspace_bytes(wd.B, wd.H, wd.kv_heads, wd.N, wd.d)
+    dsets = [(qd.to(dev), kd.to(dev), vd.to(dev), torch.empty(need, dtype=torch.uint8,
+                                                             device=dev)) for _ in range(3)]
+    dout = (torch.empty_like(dsets[0][0]),
+            torch.empty((wd.B, wd.H), dtype=torch.float32, device=dev))
+    ms, per = time_device(lambda i: fa.fa_decode(*dsets[i][:3], workspace=dsets[i][3],
+                                                 o=dout[0], lse=dout[1], scale=wd.scale),
+                          3, 10, 200, stream)
+    status.append(fa.fa_device_error())
+    nbytes = decode_bytes(wd)
+    hbm, hkind = load_hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["decode"] = {"workload": f"decode B{wd.B} H{wd.H} (K/V heads {wd.kv_heads}) "
+                                 f"N{wd.N} d{wd.d}, one query row per head",
+                     "value": gbs, "unit": "GB/s", "ms_per_step": ms, "steps": 200,
+                     "launches_per_step": 2,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm,
+                                  "frac": gbs / hbm, "peak_source": f"hbm_gbs of {hkind}",
+                                  "algorithmic_bytes": nbytes}}
+    del dsets
+
+    # latency-bound small workloads: per-call device time, and the oracle
+    # on the same inputs (all host threads, and one thread for the tiniest)
+    small = {}
+    for name, causal in (("tiny", False), ("late", False), ("late", True)):
+        w = WORKLOADS[name]
+        qc, kc, vc = make_workload(w)
+        qg, kg, vg = (t.to(dev) for t in (qc, kc, vc))
+        og = torch.empty_like(qg)
+        lg = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        ms, per = time_device(lambda i: fa.fa_fwd(qg, kg, vg, o=og, lse=lg, causal=causal,
+                                                  scale=w.scale), 1, 20, 200, stream)
+        status.append(fa.fa_device_error())
+        med = statistics.median(per)
+        # the device time without the host's submission cost: 20 calls
+        # captured in a CUDA graph, the graph replayed
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(20):
+                fa.fa_fwd(qg, kg, vg, o=og, lse=lg, causal=causal, scale=w.scale)
+        ms_graph, _ = time_device(lambda i: graph.replay(), 1, 3, 10, stream)
+        status.append(fa.fa_device_error())
+        del graph
+        nth = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.attention_fwd(qc, kc, vc, causal=causal, scale=w.scale, nthreads=nth)
+        t_all = time.perf_counter() - t0
+        key = f"{name}_{'causal' if causal else 'noncausal'}"
+        small[key] = {"workload": workload_config(w, causal)["workload"],
+                      "us_per_call_median": med * 1e3, "us_per_call_mean": ms * 1e3,
+                      "tflops_at_median": w.flops(causal) / (med * 1e-3) / 1e12,
+                      "us_per_call_graph": ms_graph / 20 * 1e3,
+                      "tflops_graph": w.flops(causal) / (ms_graph / 20 * 1e-3) / 1e12,
+                      "oracle_s": t_all, "oracle_threads": nth}
+        if name == "tiny":
+            t0 = time.perf_counter()
+            oracle.attention_fwd(qc, kc, vc, causal=causal, scale=w.scale, nthreads=1)
+            small[key]["oracle_s_one_thread"] = time.perf_counter() - t0
+    out["small"] = small
+    if any(st != 0 for st in status):
+        raise RuntimeError("device status set during a secondary leg")
+    return out
+
+
+def load_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
 
 
 # ------------------------------------------------------------ decode leg
@@ -443,11 +621,7 @@ def run_decode(args, w):
     nbytes = decode_bytes(w)
     gbs = nbytes / (ms * 1e-3) / 1e9
     flops = 4.0 * w.B * w.H * w.N * w.d
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            hbm, kind = float(json.load(f)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        hbm, kind = 6800.0, "fallback"
+    hbm, kind = load_hbm_peak()
     out = {"metric": "attn decode TFLOP/s (4·B·H·N·d) at one query row per head",
            "value": ws_ * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": ws_,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -535,6 +709,9 @@ def main(argv=None):
                     default="llama")
     ap.add_argument("--causal", choices=["auto", "0", "1"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other hot-path legs (backward, GQA, d = 256, decoding, "
+                         "small workloads) that a one-GPU run adds to its line")
     ap.add_argument("--backward", action="store_true",
                     help="time fa_bwd (gradients) instead of the forward pass")
     args = ap.parse_args(argv)
