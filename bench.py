@@ -50,9 +50,9 @@ KERNEL_SOURCES = ["online_softmax_fa_gb300/csrc/fa_fwd_sm103.cu",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_llama_traffic.json")
 
 
-def workload_config(w, causal):
+def workload_config(w, causal, kind="forward"):
     kv = f" (K/V heads {w.kv_heads})" if w.kv_heads != w.H else ""
-    return {"workload": f"{w.name} attention forward B{w.B} H{w.H}{kv} N{w.N} d{w.d}"
+    return {"workload": f"{w.name} attention {kind} B{w.B} H{w.H}{kv} N{w.N} d{w.d}"
                         + (" causal" if causal else ""),
             "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N, "d": w.d, "causal": causal,
             "scale": "1/sqrt(d) in fp32", "inputs": f"bf16 i.i.d. N(0,1), seed {w.seed}",
@@ -474,28 +474,32 @@ def secondary_legs(dev, fa, peak, peak_kind):
     out["gqa_forward"] = fwd_leg("llama_gqa", 100, e2e_steps=10)
     out["d256_forward"] = fwd_leg("d256", 100)
 
-    # backward on the llama workload (5 nominal N x N x d products)
-    w = WORKLOADS["llama"]
-    q, k, v = (t.to(dev) for t in make_workload(w))
-    do = make_grad(w.B, w.H, w.N, w.d, w.seed).to(dev)
-    o, lse = fa.fa_fwd(q, k, v, causal=True, scale=w.scale)
-    grads = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
-    wsb = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
-                      device=dev)
+    # backward (5 nominal N x N x d products) on the llama workload and at
+    # head dimension 256
+    def bwd_leg(name, steps):
+        w = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_workload(w))
+        do = make_grad(w.B, w.H, w.N, w.d, w.seed).to(dev)
+        o, lse = fa.fa_fwd(q, k, v, causal=True, scale=w.scale)
+        grads = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
+        wsb = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                          device=dev)
 
-    def bstep(i):
-        fa.fa_bwd(q, k, v, o, lse, do, *grads[i], workspace=wsb, causal=True, scale=w.scale)
-    ms, per = time_device(bstep, 2, 5, 100, stream)
-    status.append(fa.fa_device_error())
-    tf = 2.5 * w.flops(True) / (ms * 1e-3) / 1e12
-    out["backward"] = {"workload": "llama attention backward B1 H32 N8192 d128 causal",
-                       "metric": "TFLOP/s over 10*B*H*N^2*d, causal halved",
-                       "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "steps": 100,
-                       "kernel_ms_median": statistics.median(per), "launches_per_step": 3,
-                       "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
-                                    "frac": tf / peak,
-                                    "peak_source": f"bf16_tflops of {peak_kind}"}}
-    del q, k, v, do, o, lse, grads, wsb
+        def bstep(i):
+            fa.fa_bwd(q, k, v, o, lse, do, *grads[i], workspace=wsb, causal=True,
+                      scale=w.scale)
+        ms, per = time_device(bstep, 2, 3, steps, stream)
+        status.append(fa.fa_device_error())
+        tf = 2.5 * w.flops(True) / (ms * 1e-3) / 1e12
+        return {"workload": f"{name} attention backward B{w.B} H{w.H} N{w.N} d{w.d} causal",
+                "metric": "TFLOP/s over 10*B*H*N^2*d, causal halved",
+                "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+                "kernel_ms_median": statistics.median(per), "launches_per_step": 3,
+                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                             "frac": tf / peak, "peak_source": f"bf16_tflops of {peak_kind}"}}
+
+    out["backward"] = bwd_leg("llama", 100)
+    out["d256_backward"] = bwd_leg("d256", 20)
 
     # decoding: one new query row per head against an 8192-position cache
     wd = DECODE_WORKLOADS["decode"]
@@ -690,7 +694,7 @@ def run_backward(args, w, causal):
            "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": workload_config(w, causal),
+           "config": workload_config(w, causal, "backward"),
            "roofline": {"bound": "tensor", "achieved": value / ws_, "peak": peak,
                         "unit": "TFLOP/s", "frac": value / ws_ / peak,
                         "peak_source": f"bf16_tflops (burst) of {peak_kind}",

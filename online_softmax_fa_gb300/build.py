@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu",
-           "fa_decode_sm103.cu"]
+           "fa_bwd256_sm103.cu", "fa_decode_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -98,11 +98,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Shape and scalar checks shared by both entry points.
-// `fwd`: the forward entry points, which also take d = 256.
-int check_shape(int B, int H, int N, int d, float scale, bool fwd = false) {
+// Shape and scalar checks shared by the forward and backward entry points.
+int check_shape(int B, int H, int N, int d, float scale) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
-    if (d != 64 && d != 128 && !(fwd && d == 256)) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (static_cast<long long>(B) * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
     const long long qblocks = (static_cast<long long>(N) + 255) / 256;
     if (qblocks * B * H > 0x7FFFFFFFLL) return FA_ERR_SHAPE;  // grid size
@@ -143,7 +142,7 @@ extern "C" {
 int fa_fwd_gqa(const void *Q, const void *K, const void *V, void *O, float *LSE, int B,
                int H, int H_kv, int N, int d, int causal, float scale, fa_stream_t stream) {
     if (!Q || !K || !V || !O || !LSE) return FA_ERR_NULL;
-    int rc = check_shape(B, H, N, d, scale, true);
+    int rc = check_shape(B, H, N, d, scale);
     if (rc != FA_OK) return rc;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
     const auto mis16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -191,7 +190,7 @@ int fa_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int
 }
 
 size_t fa_fwd_host_gqa_workspace_bytes(int B, int H, int H_kv, int N, int d) {
-    if (check_shape(B, H, N, d, 1.f, true) != FA_OK) return 0;
+    if (check_shape(B, H, N, d, 1.f) != FA_OK) return 0;
     if (H_kv < 1 || H % H_kv != 0) return 0;
     const size_t q_bytes = static_cast<size_t>(B) * H * N * d * 2;
     const size_t kv_bytes = static_cast<size_t>(B) * H_kv * N * d * 2;
@@ -280,7 +279,7 @@ int fa_fwd_host_gqa(const void *Q_host, const void *K_host, const void *V_host,
                     int B, int H, int H_kv, int N, int d, int causal, float scale,
                     fa_stream_t stream) {
     if (!Q_host || !K_host || !V_host || !O_host || !LSE_host) return FA_ERR_NULL;
-    int rc = check_shape(B, H, N, d, scale, true);
+    int rc = check_shape(B, H, N, d, scale);
     if (rc != FA_OK) return rc;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_SHAPE;
     const size_t need = fa_fwd_host_gqa_workspace_bytes(B, H, H_kv, N, d);
@@ -565,16 +564,27 @@ int fa_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const
     }
     rc = check_arch();
     if (rc != FA_OK) return rc;
-    CUtensorMap tmQ, tmK, tmV, tmdO;
+    CUtensorMap tmQ, tmK, tmV, tmdO, tmQ64, tmK64, tmV64, tmdO64;
     const int BH = B * H;
     if (!encode_qkv_map(&tmQ, Q, BH, N, d) || !encode_qkv_map(&tmK, K, B * H_kv, N, d) ||
         !encode_qkv_map(&tmV, V, B * H_kv, N, d) || !encode_qkv_map(&tmdO, dO, BH, N, d))
+        return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
+    // d = 256 streams 64-row halves (Q, dO in the dK/dV kernel; K, V in dQ)
+    if (d == 256 && (!encode_qkv_map(&tmQ64, Q, BH, N, d, 64) ||
+                     !encode_qkv_map(&tmK64, K, B * H_kv, N, d, 64) ||
+                     !encode_qkv_map(&tmV64, V, B * H_kv, N, d, 64) ||
+                     !encode_qkv_map(&tmdO64, dO, BH, N, d, 64)))
         return fa::record_message(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed");
     fa::BwdArgs a;
     a.tmQ = &tmQ;
     a.tmK = &tmK;
     a.tmV = &tmV;
     a.tmdO = &tmdO;
+    const bool d256 = d == 256;
+    a.tmQ64 = d256 ? &tmQ64 : nullptr;
+    a.tmK64 = d256 ? &tmK64 : nullptr;
+    a.tmV64 = d256 ? &tmV64 : nullptr;
+    a.tmdO64 = d256 ? &tmdO64 : nullptr;
     a.O = O;
     a.dO = dO;
     a.LSE = LSE;
@@ -595,16 +605,18 @@ int fa_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const
 }
 
 int fa_device_error(fa_stream_t stream) {
-    int v = 0, vb = 0, vd = 0, v2 = 0;
+    int v = 0, vb = 0, vd = 0, v2 = 0, vb2 = 0;
     int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
     if (rc != FA_OK) return rc;
     rc = fa::bwd_read_and_clear_status(&vb);
+    if (rc != FA_OK) return rc;
+    rc = fa::bwd256_read_and_clear_status(&vb2);
     if (rc != FA_OK) return rc;
     rc = fa::dec_read_and_clear_status(&vd);
     if (rc != FA_OK) return rc;
     rc = fa::fwd256_read_and_clear_status(&v2);
     if (rc != FA_OK) return rc;
-    return (v == 0 && vb == 0 && vd == 0 && v2 == 0) ? FA_OK : FA_ERR_TIMEOUT;
+    return (v == 0 && vb == 0 && vd == 0 && v2 == 0 && vb2 == 0) ? FA_OK : FA_ERR_TIMEOUT;
 }
 
 int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {
@@ -623,8 +635,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_NULL: return "a required pointer is NULL";
         case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and fit the indexing)";
         case FA_ERR_HEADDIM:
-            return "head dimension not supported by this entry point (64 and 128; "
-                   "also 256 for the forward and decoding)";
+            return "head dimension not supported (64, 128 or 256)";
         case FA_ERR_ALIGN: return "Q, K, V, O must be 16-byte aligned and LSE 4-byte aligned";
         case FA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
         case FA_ERR_LAUNCH: return "a CUDA call failed";

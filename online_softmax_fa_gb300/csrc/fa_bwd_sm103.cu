@@ -977,9 +977,25 @@ static int launch_bwd_t(const BwdArgs &a) {
     return FA_OK;
 }
 
+// d = 256: the pre-pass here, the dK/dV and dQ kernels in fa_bwd256_sm103.cu.
+static int launch_bwd_256(const BwdArgs &a) {
+    const int n_blocks = (a.N + bwd::kBlk - 1) / bwd::kBlk;
+    const int Npad = n_blocks * bwd::kBlk;
+    const long long rows_pad = static_cast<long long>(a.BH) * Npad;
+    float *lse2 = a.rows, *dd = a.rows + rows_pad;
+    const long long pre_blocks = (rows_pad + 3) / 4;  // one row per warp, 4 warps per block
+    bwd::pre_kernel<256><<<static_cast<unsigned>(pre_blocks < (1 << 20) ? pre_blocks : (1 << 20)),
+                           128, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.O), static_cast<const __nv_bfloat16 *>(a.dO),
+        a.LSE, lse2, dd, a.N, Npad, rows_pad);
+    FA_CUDA_TRY(cudaGetLastError());
+    return launch_bwd256(a, lse2, dd, n_blocks);
+}
+
 int launch_bwd(const BwdArgs &a) {
     if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);
     if (a.d == 128) return a.causal ? launch_bwd_t<128, true>(a) : launch_bwd_t<128, false>(a);
+    if (a.d == 256) return launch_bwd_256(a);
     return FA_ERR_HEADDIM;
 }
 

@@ -33,6 +33,7 @@ int fwd256_read_and_clear_status(int *status);
 // Backward pass (fa_bwd_sm103.cu).
 struct BwdArgs {
     const CUtensorMap *tmQ, *tmK, *tmV, *tmdO;
+    const CUtensorMap *tmQ64, *tmK64, *tmV64, *tmdO64;  // d = 256: 64-row boxes (else null)
     const void *O, *dO;          // bf16 [BH, N, d]
     const float *LSE;            // fp32 [BH, N] (natural log)
     float *rows;                 // fp32 scratch [2][BH][Npad]: LSE*log2(e), rowsum(dO*O)
@@ -47,6 +48,10 @@ struct BwdArgs {
 };
 int launch_bwd(const BwdArgs &a);
 int bwd_read_and_clear_status(int *status);
+// d = 256 dK/dV and dQ kernels (fa_bwd256_sm103.cu), after the pre-pass
+// has written the padded -LSE*log2(e) and -D rows.
+int launch_bwd256(const BwdArgs &a, const float *lse2, const float *dd, int n_blocks);
+int bwd256_read_and_clear_status(int *status);
 
 // Split-KV decoding (fa_decode_sm103.cu).
 struct DecodeArgs {

@@ -61,7 +61,7 @@ def _load():
                                         ctypes.c_int, ctypes.c_double, p, i64,
                                         ctypes.c_int]
         lib.fa_oracle_fwd_q.restype = ctypes.c_int
-        lib.fa_oracle_bwd.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int,
+        lib.fa_oracle_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int,
                                       ctypes.c_double, ctypes.c_int]
         lib.fa_oracle_bwd.restype = ctypes.c_int
         lib.fa_oracle_fwd_blockwise.argtypes = [
@@ -202,10 +202,12 @@ def attention_decode(q, k, v, causal: bool = True, scale: float | None = None,
 
 
 def attention_bwd(q, k, v, do, causal: bool = False, scale: float | None = None,
-                  nthreads: int | None = None, return_D: bool = False):
+                  nthreads: int | None = None, return_D: bool = False, D=None):
     """Gradients (dQ, dK, dV) of the forward pass for the output gradient
     dO, by the definition (fp64, S, P, dP, dS materialised per head).
-    q, k, v, do: [..., N, d].  With ``return_D`` also D_i = sum_r dO_ir O_ir."""
+    q, k, v, do: [..., N, d].  With ``return_D`` also D_i = sum_r dO_ir O_ir.
+    ``D`` ([..., N], optional) replaces the D_i of the exact O: the same
+    gradients with D taken from another O (e.g. the forward's bf16 output)."""
     q, k, v, do = (_as_f64(x, n) for x, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")))
     if not (q.shape == k.shape == v.shape == do.shape) or q.ndim < 2:
         raise ValueError("q, k, v, do must share one shape [..., N, d]")
@@ -215,11 +217,15 @@ def attention_bwd(q, k, v, do, causal: bool = False, scale: float | None = None,
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     dq, dk, dv = (np.empty((BH, N, d)) for _ in range(3))
+    D_in = None
+    if D is not None:
+        D_in = np.ascontiguousarray(np.asarray(D, dtype=np.float64).reshape(BH, N))
     D = np.empty((BH, N))
     q, k, v, do = (np.ascontiguousarray(x) for x in (q, k, v, do))
     rc = _load().fa_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
-                               _ptr(dv), _ptr(D), BH, N, d, 1 if causal else 0,
-                               float(scale), nthreads or default_threads())
+                               _ptr(dv), _ptr(D), _ptr(D_in) if D_in is not None else None,
+                               BH, N, d, 1 if causal else 0, float(scale),
+                               nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"fa_oracle_bwd failed ({rc})")
     out = (dq.reshape(q.shape), dk.reshape(q.shape), dv.reshape(q.shape))
@@ -229,7 +235,7 @@ def attention_bwd(q, k, v, do, causal: bool = False, scale: float | None = None,
 
 
 def attention_bwd_gqa(q, k, v, do, causal: bool = False, scale: float | None = None,
-                      nthreads: int | None = None):
+                      nthreads: int | None = None, D=None):
     """Gradients (dQ, dK, dV) of grouped-query attention ("Understanding
     FlashAttention Pt 1", section 4.1: query head h uses K/V head
     h // (H / H_kv)) for the output gradient dO.  q, do [B, H, N, d]; k, v
@@ -248,7 +254,7 @@ def attention_bwd_gqa(q, k, v, do, causal: bool = False, scale: float | None = N
     k_full = np.repeat(k, group, axis=1)
     v_full = np.repeat(v, group, axis=1)
     dq, dk_full, dv_full = attention_bwd(q, k_full, v_full, do, causal=causal, scale=scale,
-                                         nthreads=nthreads)
+                                         nthreads=nthreads, D=D)
     dk = dk_full.reshape(B, H_kv, group, N, d).sum(axis=2)
     dv = dv_full.reshape(B, H_kv, group, N, d).sum(axis=2)
     return dq, dk, dv

@@ -338,12 +338,18 @@ int fa_oracle_fwd_blockwise(const double *Q, const double *K, const double *V,
  *   O = P V, dV = P^T dO, dP = dO V^T, D_i = sum_r dO_ir O_ir,
  *   dS = P * (dP - D_i), dQ = scale * dS K, dK = scale * dS^T Q.
  * O is recomputed here from Q, K, V (not taken from the caller).
- * Layouts: Q, K, V, dO, dQ, dK, dV are [BH, N, d] fp64; D_out (optional,
- * may be NULL) is [BH, N].  Returns 0, -1 (bad argument) or -2 (memory).
+ * D_in (optional, may be NULL) replaces the D_i computed from that exact O
+ * by the caller's values: the same gradients with D taken from another O,
+ * e.g. the forward's output rounded to bf16 (tests use it to size the
+ * effect of that rounding on the gradients).
+ * Layouts: Q, K, V, dO, dQ, dK, dV are [BH, N, d] fp64; D_out and D_in
+ * (optional, may be NULL) are [BH, N].  Returns 0, -1 (bad argument) or -2
+ * (memory).
  */
 typedef struct {
     const double *Q, *K, *V, *dO;
     double *dQ, *dK, *dV, *D_out;
+    const double *D_in;
     int64_t BH, N, d;
     int causal;
     double scale;
@@ -387,6 +393,7 @@ static void bwd_head(bwd_job *jb, int64_t bh, double *S, double *P, double *dP) 
             for (int64_t j = 0; j < N; ++j) o += P[i * N + j] * V[j * d + c];
             Di += dO[i * d + c] * o;
         }
+        if (jb->D_in) Di = jb->D_in[bh * N + i];
         if (jb->D_out) jb->D_out[bh * N + i] = Di;
         /* dS overwrites dP */
         for (int64_t j = 0; j < N; ++j) dP[i * N + j] = P[i * N + j] * (dP[i * N + j] - Di);
@@ -432,14 +439,14 @@ static void *bwd_worker(void *arg) {
 }
 
 int fa_oracle_bwd(const double *Q, const double *K, const double *V, const double *dO,
-                  double *dQ, double *dK, double *dV, double *D_out, int64_t BH, int64_t N,
-                  int64_t d, int causal, double scale, int nthreads) {
+                  double *dQ, double *dK, double *dV, double *D_out, const double *D_in,
+                  int64_t BH, int64_t N, int64_t d, int causal, double scale, int nthreads) {
     if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return -1;
     if (BH < 1 || N < 1 || d < 1) return -1;
     bwd_job jb;
     memset(&jb, 0, sizeof jb);
     jb.Q = Q; jb.K = K; jb.V = V; jb.dO = dO;
-    jb.dQ = dQ; jb.dK = dK; jb.dV = dV; jb.D_out = D_out;
+    jb.dQ = dQ; jb.dK = dK; jb.dV = dV; jb.D_out = D_out; jb.D_in = D_in;
     jb.BH = BH; jb.N = N; jb.d = d; jb.causal = causal ? 1 : 0; jb.scale = scale;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > BH) nthreads = (int)BH;

@@ -68,11 +68,14 @@ def test_bad_shapes(lib):
 
 
 def test_head_dim_256(lib):
-    # the forward and decoding take d = 256 (checks pass up to the device
-    # check); the backward does not
+    # the forward, the backward and decoding take d = 256 (checks pass up to
+    # the device check); other head dimensions are rejected
     assert _call(lib, Q=1 << 20, K=2 << 20, V=3 << 20, O=4 << 20, L=5 << 20, d=256) in (0, -5)
-    assert lib.fa_bwd_workspace_bytes(1, 1, 8, 256) == 0
+    # the backward's workspace does not depend on d: two fp32 per padded row
+    assert lib.fa_bwd_workspace_bytes(1, 1, 8, 256) == lib.fa_bwd_workspace_bytes(1, 1, 8, 128) > 0
     assert lib.fa_decode_workspace_bytes(1, 1, 1, 8, 256) > 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 8, 96) == 0
+    assert _call(lib, d=96) == -3
 
 
 def test_bad_scale(lib):
@@ -139,10 +142,10 @@ def test_gqa_argument_checks(lib):
 def test_bwd_gqa_argument_checks(lib):
     # Q K V O dO LSE dQ dK dV workspace bytes
     base = (16, 32, 48, 64, 80, 96, 4096, 8192, 12288, 65536, 1 << 30)
-    # H_kv must divide H and be >= 1; head dimension 64 or 128; null pointers
+    # H_kv must divide H and be >= 1; head dimension 64, 128 or 256; null pointers
     assert lib.fa_bwd_gqa(*base, 1, 8, 3, 8, 64, 0, 0.125, None) == -2
     assert lib.fa_bwd_gqa(*base, 1, 8, 0, 8, 64, 0, 0.125, None) == -2
-    assert lib.fa_bwd_gqa(*base, 1, 8, 2, 8, 256, 0, 0.0625, None) == -3
+    assert lib.fa_bwd_gqa(*base, 1, 8, 2, 8, 96, 0, 0.125, None) == -3
     assert lib.fa_bwd_gqa(None, *base[1:], 1, 8, 2, 8, 64, 0, 0.125, None) == -1
 
 

@@ -452,3 +452,26 @@ def test_backward_identities():
         _, _, dv1 = oracle.attention_bwd(q, k, v, np.ones_like(do), causal=causal, scale=0.3)
         if not causal:
             np.testing.assert_allclose(dv1.sum(axis=1), 40.0 * np.ones((2, 8)), atol=1e-10)
+
+
+def test_backward_with_given_D():
+    """The backward's optional D input (section 3.6's D_i = sum_r dO_ir O_ir
+    taken from another O): the exact D reproduces the default bit for bit,
+    and a shift delta_i of D_i leaves dV unchanged and moves dQ_i by
+    -scale * delta_i * sum_j P_ij K_j, which is the forward pass with K in
+    place of V (dS_ij moves by -P_ij delta_i)."""
+    g = np.random.default_rng(17)
+    B, H, N, d = 1, 2, 9, 5
+    q, k, v, do = (g.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 0.4
+    for causal in (False, True):
+        dq, dk, dv, D = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale,
+                                             return_D=True)
+        dq2, dk2, dv2 = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale, D=D)
+        assert np.array_equal(dq, dq2) and np.array_equal(dk, dk2) and np.array_equal(dv, dv2)
+        delta = g.standard_normal((B, H, N)) * 0.1
+        dq3, dk3, dv3 = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale,
+                                             D=D + delta)
+        assert np.allclose(dv3, dv, rtol=0, atol=1e-13)
+        wk, _ = oracle.attention_fwd(q, k, k, causal=causal, scale=scale)  # sum_j P_ij K_j
+        assert np.allclose(dq3 - dq, -scale * delta[..., None] * wk, rtol=0, atol=1e-12)
