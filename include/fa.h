@@ -174,7 +174,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                   the same Q, K, V, causal and scale), device, read
  *   LSE             fp32 [B, H, N], device, read
  *   dQ, dK, dV      bf16 [B, H, N, d], device, written
- *   d               64 or 128 (FA_ERR_HEADDIM for 256: the forward only)
+ *   d               64, 128 or 256 (at 256 other kernels run: dK / dV by two
+ *                   CTAs per key block, one per half of d, and the query or
+ *                   key rows streamed in 64-row halves; correct and
+ *                   deterministic, about a third of the d <= 128 rate)
  *   workspace       caller-owned device scratch of at least
  *                   fa_bwd_workspace_bytes(B, H, N, d) bytes, 256-byte aligned
  * Three kernels on `stream` (D, then dK/dV with key blocks outermost, then
