@@ -194,10 +194,16 @@ def oracle_sample(w, causal, q, k, v, rows_per_head, nthreads, offset=0):
 
 
 def oracle_inputs(w):
+    """Q, K, V in fp64 as [B*H, N, d]; grouped-query K/V heads are repeated
+    for the query heads of their group (query head h uses K/V head
+    h // (H / H_kv)), so the dense oracle sees the same attention."""
     import oracle
     q, k, v = make_workload(w)
     BH = w.B * w.H
     shp = (BH, w.N, w.d)
+    group = w.H // w.kv_heads
+    if group > 1:
+        k, v = (t.repeat_interleave(group, dim=1) for t in (k, v))
     return tuple(oracle.bf16_bits_to_f64(t.reshape(shp)) for t in (q, k, v))
 
 
@@ -473,6 +479,32 @@ def secondary_legs(dev, fa, peak, peak_kind):
 
     out["gqa_forward"] = fwd_leg("llama_gqa", 100, e2e_steps=10)
     out["d256_forward"] = fwd_leg("d256", 100)
+    # the other two full-size configurations, each with the oracle timed on
+    # a bounded sample of its rows (the batch workload: 16 rows per head;
+    # the long one: its parity sample, 512 seeded rows per head and the edge
+    # rows, all of which attend to up to 32771 keys)
+    for name, rph in (("batch", 16), ("long", 0)):
+        w = WORKLOADS[name]
+        causal = w.causal[-1]
+        leg = fwd_leg(name, 50 if name == "batch" else 20)
+        qf, kf, vf = oracle_inputs(w)
+        nth = oracle.default_threads()
+        if rph:
+            dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth)
+            what = f"{rph} evenly spaced rows in each of the {w.B * w.H} heads"
+        else:
+            from online_softmax_fa_gb300.inputs import sample_rows
+            rows = sample_rows(w.N, w.B * w.H, w.sampled_rows, seed=w.seed)
+            t0 = time.perf_counter()
+            oracle.attention_fwd(qf, kf, vf, causal=causal, scale=w.scale, rows=rows,
+                                 nthreads=nth)
+            dt = time.perf_counter() - t0
+            fl = row_flops(rows, w.N, w.d, causal)
+            what = f"the parity sample: {rows.shape[1]} rows in each of the {w.B * w.H} heads"
+        leg["oracle"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "seconds": dt,
+                         "cores": nth, "sample": what}
+        out[f"{name}_forward"] = leg
+        del qf, kf, vf
 
     # backward (5 nominal N x N x d products) on the llama workload and at
     # head dimension 256
