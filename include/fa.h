@@ -45,7 +45,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = -8, /* valid request this library does not implement */
     FA_ERR_SCALE = -9,       /* scale is not a finite number > 0 */
     FA_ERR_ALIAS = -10,      /* an output buffer overlaps an input buffer */
-    FA_ERR_WORKSPACE = -11   /* workspace too small or misaligned */
+    FA_ERR_WORKSPACE = -11,  /* workspace too small or misaligned */
+    FA_ERR_CHECK = -12       /* a device index check failed (debug build, fa_debug.h) */
 } fa_status;
 
 /*
@@ -284,10 +285,25 @@ int fa_decode_noalloc(const void *Q, const void *K, const void *V, void *O, floa
  * FA_ERR_TIMEOUT if a kernel since the last call gave up on a bounded wait
  * (every wait inside the kernels has a time limit; on expiry the kernel
  * drains its own copies, frees its tensor memory and exits early, leaving
- * its outputs undefined), or FA_ERR_LAUNCH if the synchronisation itself
- * reported a CUDA error.
+ * its outputs undefined), FA_ERR_CHECK if a device index check of the debug
+ * build failed (a timeout caused by it is not reported separately), or
+ * FA_ERR_LAUNCH if the synchronisation itself reported a CUDA error.
  */
 int fa_device_error(fa_stream_t stream);
+
+/*
+ * fa_last_device_status -- the raw device status behind the calling
+ * thread's last fa_device_error (or fa_selftest_bounded_wait) result: 0 if
+ * that returned FA_OK, else (kernel << 8) | code for the first kernel, in
+ * the order below, whose status word was set:
+ *   kernel  1 forward (d 64, 128)   2 forward (d 256)   3 backward (d 64, 128)
+ *           4 backward (d 256)      5 decoding
+ *   code    1 .. 127: the bounded wait that ran out (each kernel numbers
+ *           its own waits; 127 is the self-test's wait);
+ *           0x80 | n: device check n failed (debug build, fa_debug.h).
+ * Host-only; never fails.
+ */
+int fa_last_device_status(void);
 
 /*
  * fa_selftest_bounded_wait -- runs a one-CTA kernel that waits on a barrier

@@ -3,6 +3,10 @@
 Each translation unit compiles in its own nvcc process (in parallel), then
 one nvcc call links the shared library.  No CMake, no torch extension
 machinery: the library exports the plain C ABI of ``include/fa.h``.
+
+The same call builds the debug library ``_build/libfa_gb300_debug.so``: the
+release objects with the forward kernel's unit recompiled with ``FA_DEBUG``
+(device index checks and the fault knobs of ``include/fa_debug.h``).
 """
 from __future__ import annotations
 
@@ -16,6 +20,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300.so")
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300_debug.so")
+DEBUG_SOURCES = ["fa_fwd_sm103.cu"]  # recompiled with FA_DEBUG for the debug library
 SOURCES = ["fa_api.cu", "fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu",
            "fa_bwd256_sm103.cu", "fa_decode_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -30,41 +36,54 @@ def nvcc_path() -> str:
 
 def _inputs_mtime() -> float:
     paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    paths.append(os.path.join(ROOT, "include", "fa.h"))
+    inc = os.path.join(ROOT, "include")
+    paths += [os.path.join(inc, f) for f in os.listdir(inc)]
     paths.append(os.path.abspath(__file__))
     return max(os.path.getmtime(p) for p in paths)
 
 
 def build_library(force: bool = False, verbose_ptxas: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
-    if (not force and os.path.exists(LIB_PATH)
-            and os.path.getmtime(LIB_PATH) >= _inputs_mtime()):
-        return LIB_PATH
+    if not force:
+        newest = _inputs_mtime()
+        if all(os.path.exists(p) and os.path.getmtime(p) >= newest
+               for p in (LIB_PATH, DEBUG_LIB_PATH)):
+            return LIB_PATH
     nvcc = nvcc_path()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", os.path.join(ROOT, "include")]
     if verbose_ptxas:
         common += ["-Xptxas", "-v"]
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, debug = job
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", "_debug.o" if debug else ".o"))
+        cmd = [nvcc] + common + (["-DFA_DEBUG"] if debug else [])
+        cmd += ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-        return obj, r.stdout + r.stderr
+        return src, debug, obj, r.stdout + r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    jobs = [(s, False) for s in SOURCES] + [(s, True) for s in DEBUG_SOURCES]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(compile_one, jobs))
     if verbose_ptxas:
-        for _, log in results:
-            print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+        for src, debug, _, log in results:
+            print(f"== {src}{' (FA_DEBUG)' if debug else ''}\n{log}")
+    release = {src: obj for src, debug, obj, _ in results if not debug}
+    debug_objs = {src: obj for src, debug, obj, _ in results if debug}
+
+    def link(objs, path):
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, path)
+
+    link([release[s] for s in SOURCES], LIB_PATH)
+    link([debug_objs.get(s, release[s]) for s in SOURCES], DEBUG_LIB_PATH)
     return LIB_PATH
 
 

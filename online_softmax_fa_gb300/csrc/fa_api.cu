@@ -110,6 +110,7 @@ int check_shape(int B, int H, int N, int d, float scale) {
 }
 
 thread_local char g_detail[256] = "";
+thread_local int g_last_status = 0;  // raw status behind the last fa_device_error
 
 }  // namespace
 
@@ -605,19 +606,28 @@ int fa_bwd_gqa(const void *Q, const void *K, const void *V, const void *O, const
 }
 
 int fa_device_error(fa_stream_t stream) {
-    int v = 0, vb = 0, vd = 0, v2 = 0, vb2 = 0;
-    int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
+    g_last_status = 0;
+    // status words in the order of fa_last_device_status's kernel numbers
+    int w[5] = {0, 0, 0, 0, 0};
+    int rc = fa::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &w[0]);
     if (rc != FA_OK) return rc;
-    rc = fa::bwd_read_and_clear_status(&vb);
+    rc = fa::fwd256_read_and_clear_status(&w[1]);
     if (rc != FA_OK) return rc;
-    rc = fa::bwd256_read_and_clear_status(&vb2);
+    rc = fa::bwd_read_and_clear_status(&w[2]);
     if (rc != FA_OK) return rc;
-    rc = fa::dec_read_and_clear_status(&vd);
+    rc = fa::bwd256_read_and_clear_status(&w[3]);
     if (rc != FA_OK) return rc;
-    rc = fa::fwd256_read_and_clear_status(&v2);
+    rc = fa::dec_read_and_clear_status(&w[4]);
     if (rc != FA_OK) return rc;
-    return (v == 0 && vb == 0 && vd == 0 && v2 == 0 && vb2 == 0) ? FA_OK : FA_ERR_TIMEOUT;
+    for (int k = 0; k < 5; ++k) {
+        if (w[k] == 0) continue;
+        g_last_status = ((k + 1) << 8) | (w[k] & 0xFF);
+        return (w[k] & 0x80) ? FA_ERR_CHECK : FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
 }
+
+int fa_last_device_status(void) { return g_last_status; }
 
 int fa_selftest_bounded_wait(int limit_us, fa_stream_t stream) {
     if (limit_us < 1 || limit_us > 1000000) return FA_ERR_SHAPE;
@@ -644,6 +654,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_SCALE: return "scale must be a finite number > 0";
         case FA_ERR_ALIAS: return "an output buffer overlaps an input buffer";
         case FA_ERR_WORKSPACE: return "workspace NULL, too small or not 256-byte aligned";
+        case FA_ERR_CHECK: return "a device index check failed (debug build)";
         default: return "unknown status";
     }
 }

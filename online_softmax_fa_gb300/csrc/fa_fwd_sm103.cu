@@ -58,6 +58,11 @@
 
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
+#ifdef FA_DEBUG
+#include <mutex>
+
+#include "../../include/fa_debug.h"
+#endif
 
 namespace fa {
 
@@ -95,6 +100,33 @@ enum : int {
     kSiteSFull, kSiteOFull, kSiteQEmpty, kSiteOEmpty, kSiteSchedFull, kSiteSchedEmpty,
     kSiteClaim
 };
+
+// Device checks of the debug build (compiled with FA_DEBUG).  Every index the
+// kernel computes is checked before use; a failed check records 0x80 | its
+// number in the status word (first error wins), raises the CTA's abort flag
+// and skips the access, so the CTA's other warps stop at their next wait that
+// does not complete at once.  No check traps.  Release builds compile every
+// check to `true`.
+enum : int {
+    kChkItem = 1,  // work item id outside [0, n_items)
+    kChkTmaQ,      // Q box rows outside the padded query rows, or head >= B*H
+    kChkTmaKV,     // K/V box starting at or past N, or K/V head >= B*H_kv
+    kChkSmem,      // a shared-memory range outside the CTA's allocation
+    kChkTmem,      // tensor memory not the whole 512-column allocation
+    kChkStoreO,    // an O store outside the output, or misaligned for its width
+    kChkStoreLse   // an LSE store outside the output
+};
+#ifdef FA_DEBUG
+constexpr bool kDebug = true;
+__device__ __forceinline__ bool dbg_ok(bool cond, const WaitCtl &c, int check) {
+    if (cond) return true;
+    raise_abort(c, 0x80 | check);
+    return false;
+}
+#else
+constexpr bool kDebug = false;
+__device__ __forceinline__ bool dbg_ok(bool, const WaitCtl &, int) { return true; }
+#endif
 
 template <int D>
 struct Cfg {
@@ -158,6 +190,11 @@ struct Params {
     float scale_log2;  // scale * log2(e)
     uint64_t limit_ns;
     int o_align32;     // O is 32-byte aligned: the epilogue stores 32 bytes at a time
+    // debug build only: the extent (rows of O and LSE) the store checks
+    // use, and an injected fault -- the producer of item lose_item skips the
+    // load of key tile lose_tile and the arrival on its barrier (-1: none)
+    long long o_rows;
+    int lose_item, lose_tile;
 };
 
 // Shared-memory layout of one CTA (rebuilt where needed: it costs a few
@@ -205,6 +242,16 @@ __device__ __forceinline__ SmemView<D> smem_view() {
     v.sched_item = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);
     v.claim_resp = smem + C::kOffMisc + 16;
     return v;
+}
+
+// Debug checks: [ptr, ptr + bytes) lies inside the CTA's aligned shared
+// memory, below the 256 KB a descriptor's 14-bit address field reaches.
+template <int D>
+__device__ __forceinline__ bool in_smem(const void *ptr, int bytes) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw), a = smem_u32(ptr);
+    const uint32_t end = base + static_cast<uint32_t>(Cfg<D>::kSmemBytes);
+    return a >= base && a + static_cast<uint32_t>(bytes) <= end && a + bytes <= (1u << 18);
 }
 
 // ------------------------------------------------------------- schedule
@@ -259,12 +306,13 @@ __device__ __forceinline__ Work work_of(const Params &p, int x) {
 // slot.
 template <int D>
 __device__ __forceinline__ bool next_item(const SmemView<D> &v, const WaitCtl &ctl, int r,
-                                          int lane, int &x) {
+                                          int lane, int n_items, int &x) {
     const int slot = r & 1;
     if (!__all_sync(0xffffffffu, mbar_wait(&v.sched_full[slot], (r >> 1) & 1, ctl,
                                            kSiteSchedFull)))
         return false;
     x = v.sched_item[slot];
+    if (x >= 0 && !dbg_ok(x < n_items, ctl, kChkItem)) x = -1;
     __syncwarp();
     if (lane == 0) mbar_arrive(&v.sched_empty[slot]);
     return true;
@@ -294,6 +342,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
             ok = mbar_wait(&v.sched_empty[slot], ((r >> 1) & 1) ^ 1, ctl, kSiteSchedEmpty);
             if (!ok) break;
         }
+        if (x >= 0 && !dbg_ok(x < p.n_items, ctl, kChkItem)) x = -1;  // end the work
         v.sched_item[slot] = x;
         mbar_arrive(&v.sched_full[slot]);
         if (x < 0) break;
@@ -301,6 +350,12 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
         if (r > 0) {  // the previous item's last S MMA has read Q
             ok = mbar_wait(v.q_empty, (r - 1) & 1, ctl, kSiteQEmpty);
             if (!ok) break;
+        }
+        if (!dbg_ok(w.bh >= 0 && w.bh < p.BH && w.qb >= 0 && w.qb < p.n_qblocks, ctl,
+                    kChkTmaQ) ||
+            !dbg_ok(in_smem<D>(v.q, C::kQBytes), ctl, kChkSmem)) {
+            ok = false;
+            break;
         }
         mbar_arrive_expect_tx(v.q_full, C::kQBytes);
         {
@@ -326,10 +381,23 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
                 g = t;
                 break;
             }
-            mbar_arrive_expect_tx(&v.k_full[s], C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(v.k + s * C::kTileBytes + c * kBoxBytes, tmK, &v.k_full[s], 64 * c,
-                            j * kBlockN, w.kvh, pol_kv);
+            if (!dbg_ok(j * kBlockN < p.N && w.kvh >= 0 && w.kvh < p.BH / p.group, ctl,
+                        kChkTmaKV) ||
+                !dbg_ok(in_smem<D>(v.k + s * C::kTileBytes, C::kTileBytes) &&
+                            in_smem<D>(v.v + s * C::kTileBytes, C::kTileBytes),
+                        ctl, kChkSmem)) {
+                ok = false;
+                g = t;
+                break;
+            }
+            // debug build: an injected fault loses this tile's K load and
+            // its arrival (the consumers' waits then run out)
+            if (!(kDebug && x == p.lose_item && j == p.lose_tile)) {
+                mbar_arrive_expect_tx(&v.k_full[s], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(v.k + s * C::kTileBytes + c * kBoxBytes, tmK, &v.k_full[s],
+                                64 * c, j * kBlockN, w.kvh, pol_kv);
+            }
             if (t >= C::kStages) ok = mbar_wait(&v.v_empty[s], ph ^ 1, ctl, kSiteVEmpty);
             if (!ok) {  // K of tile t is in flight: count it for the drain
                 g = t + 1;
@@ -389,10 +457,15 @@ __device__ __forceinline__ void role_mma(const Params &p) {
     const int lane = static_cast<int>(threadIdx.x & 31);
     int g = 0;             // K/V tiles consumed, across items
     int pc0 = 0, pc1 = 0;  // P tiles consumed per sub-tile, across items
-    bool ok = true;
+    bool ok = dbg_ok((tmem & 0xFFFFu) + kTmemCols <= 512u && (tmem >> 16) == 0u, ctl,
+                     kChkTmem) &&
+              dbg_ok(in_smem<D>(v.q, C::kQBytes) &&
+                         in_smem<D>(v.k, C::kStages * C::kTileBytes) &&
+                         in_smem<D>(v.v, C::kStages * C::kTileBytes),
+                     ctl, kChkSmem);
     for (int r = 0; ok; ++r) {
         int x;
-        ok = next_item(v, ctl, r, lane, x);
+        ok = next_item(v, ctl, r, lane, p.n_items, x);
         if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int n0 = w.n_sub0, n1 = w.n_sub1;
@@ -504,10 +577,11 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
     const uint64_t cs2 = f2_pack(cs, cs);
 
     int sc = 0;  // S tiles consumed, across items
-    bool ok = true;
+    bool ok = dbg_ok((tmem & 0xFFFFu) + kTmemCols <= 512u && (tmem >> 16) == 0u, ctl,
+                     kChkTmem);
     for (int r = 0; ok; ++r) {
         int x;
-        ok = next_item(v, ctl, r, lane, x);
+        ok = next_item(v, ctl, r, lane, p.n_items, x);
         if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int sub_start = w.qb * kBlockM + k * kSubM;
@@ -603,6 +677,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const bool in_range = qrow < N;
+        const long long row_flat = static_cast<long long>(w.bh) * N + qrow;
         __nv_bfloat16 *orow = p.O + (static_cast<size_t>(w.bh) * N + qrow) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -613,7 +688,11 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
             for (int t = 0; t < 16; ++t)
                 pk[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l,
                                     __uint_as_float(o[2 * t + 1]) * inv_l);
-            if (in_range) {
+            if (in_range &&
+                dbg_ok(row_flat < p.o_rows &&
+                           (reinterpret_cast<uintptr_t>(orow + 32 * c) &
+                            (p.o_align32 ? 31u : 15u)) == 0,
+                       ctl, kChkStoreO)) {
                 if (p.o_align32) {
                     st_global_v8(orow + 32 * c, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6],
                                  pk[7]);
@@ -632,7 +711,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
-        if (in_range) {
+        if (in_range && dbg_ok(row_flat < p.o_rows, ctl, kChkStoreLse)) {
             const float lse = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
             p.LSE[static_cast<size_t>(w.bh) * N + qrow] = lse;
         }
@@ -726,6 +805,27 @@ __global__ void fa_wait_selftest_kernel(uint64_t limit_ns) {
     }
 }
 
+#ifdef FA_DEBUG
+// The fault fa_debug_arm armed for the next launch (debug build only).
+static std::mutex g_arm_mu;
+static int g_arm_fault = FA_DEBUG_NONE;
+static long long g_arm_a = 0, g_arm_b = 0;
+static uint64_t g_arm_limit_ns = 0;
+
+static void take_armed_fault(Params &p) {
+    std::lock_guard<std::mutex> lock(g_arm_mu);
+    if (g_arm_fault == FA_DEBUG_NONE) return;
+    if (g_arm_fault == FA_DEBUG_LOSE_K_ARRIVAL) {
+        p.lose_item = g_arm_a > 0x7FFFFFFFLL ? -1 : static_cast<int>(g_arm_a);
+        p.lose_tile = g_arm_b > 0x7FFFFFFFLL ? -1 : static_cast<int>(g_arm_b);
+    } else if (g_arm_fault == FA_DEBUG_SHRINK_OUTPUT) {
+        p.o_rows = g_arm_a < p.o_rows ? g_arm_a : p.o_rows;
+    }
+    if (g_arm_limit_ns) p.limit_ns = g_arm_limit_ns;
+    g_arm_fault = FA_DEBUG_NONE;
+}
+#endif
+
 template <int D, bool CAUSAL>
 static int launch_t(const LaunchArgs &a) {
     using C = Cfg<D>;
@@ -753,6 +853,12 @@ static int launch_t(const LaunchArgs &a) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
     p.o_align32 = (reinterpret_cast<uintptr_t>(a.O) & 31u) == 0 ? 1 : 0;
+    p.o_rows = static_cast<long long>(a.BH) * a.N;
+    p.lose_item = -1;
+    p.lose_tile = -1;
+#ifdef FA_DEBUG
+    take_armed_fault(p);
+#endif
     // Causal head groups: each group holds about two waves of its heaviest
     // items (a head brings n_qblocks items, the heaviest twice the average),
     // whole K/V groups of grouped-query heads, at most all heads.
@@ -795,3 +901,18 @@ int launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
 }
 
 }  // namespace fa
+
+#ifdef FA_DEBUG
+extern "C" int fa_debug_arm(int fault, long long a, long long b, int limit_us) {
+    if (fault != FA_DEBUG_NONE && fault != FA_DEBUG_LOSE_K_ARRIVAL &&
+        fault != FA_DEBUG_SHRINK_OUTPUT)
+        return FA_ERR_UNSUPPORTED;
+    if (a < 0 || b < 0 || limit_us < 0 || limit_us > 1000000) return FA_ERR_SHAPE;
+    std::lock_guard<std::mutex> lock(fa::g_arm_mu);
+    fa::g_arm_fault = fault;
+    fa::g_arm_a = a;
+    fa::g_arm_b = b;
+    fa::g_arm_limit_ns = fault == FA_DEBUG_NONE ? 0 : static_cast<uint64_t>(limit_us) * 1000ull;
+    return FA_OK;
+}
+#endif

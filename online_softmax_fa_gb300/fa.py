@@ -13,11 +13,18 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libfa_gb300_debug.so")
 
 FA_OK = 0
 FA_ERR_TIMEOUT = -7
+FA_ERR_CHECK = -12
+# include/fa_debug.h
+FA_DEBUG_NONE = 0
+FA_DEBUG_LOSE_K_ARRIVAL = 1
+FA_DEBUG_SHRINK_OUTPUT = 2
 
 _lib = None
+_debug_lib = None
 
 
 class FaError(RuntimeError):
@@ -33,7 +40,25 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    _lib = _open(path or LIB_PATH)
+    return _lib
+
+
+def load_debug_library() -> ctypes.CDLL:
+    """Load (once) the debug build (include/fa_debug.h): a handle of its own,
+    with every fa.h function plus fa_debug_arm.  The module-level functions
+    below keep using the release library."""
+    global _debug_lib
+    if _debug_lib is None:
+        lib = _open(DEBUG_LIB_PATH)
+        lib.fa_debug_arm.argtypes = [ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong,
+                                     ctypes.c_int]
+        lib.fa_debug_arm.restype = ctypes.c_int
+        _debug_lib = lib
+    return _debug_lib
+
+
+def _open(path: str) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise RuntimeError(
             f"CUDA library not found at {path}; build it with "
@@ -74,7 +99,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.fa_last_error_detail.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = I
-    _lib = lib
+    lib.fa_last_device_status.argtypes = []
+    lib.fa_last_device_status.restype = I
     return lib
 
 
@@ -301,6 +327,11 @@ def fa_decode(q, k, v, workspace=None, o=None, lse=None, scale: float | None = N
 
 def fa_device_error(stream=None) -> int:
     return int(load_library().fa_device_error(_stream_handle(stream)))
+
+
+def fa_last_device_status() -> int:
+    """(kernel << 8) | code behind this thread's last fa_device_error; 0 if clean."""
+    return int(load_library().fa_last_device_status())
 
 
 def fa_selftest_bounded_wait(limit_us: int, stream=None) -> int:

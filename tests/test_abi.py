@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     from online_softmax_fa_gb300 import fa
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(-999) == "unknown status"
@@ -117,6 +117,36 @@ def test_valid_request_without_gpu_reports_arch(lib):
     assert _call(lib, Q=1 << 20, K=2 << 20, V=3 << 20, O=4 << 20, L=5 << 20) == -5
     assert lib.fa_selftest_bounded_wait(1000, None) == -5
     assert lib.fa_selftest_bounded_wait(0, None) == -2
+
+
+def declared_debug_functions():
+    src = open(os.path.join(ROOT, "include", "fa_debug.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", src, re.M)))
+
+
+def test_debug_library_exports(lib):
+    """The debug build exports fa.h and fa_debug.h; the release build only fa.h."""
+    from online_softmax_fa_gb300 import fa
+    dbg = fa.load_debug_library()
+    assert declared_debug_functions() == ["fa_debug_arm"]
+    for name in declared_functions() + declared_debug_functions():
+        assert hasattr(dbg, name), name
+    assert not hasattr(lib, "fa_debug_arm")
+
+
+def test_debug_arm_checks(lib):
+    from online_softmax_fa_gb300 import fa
+    dbg = fa.load_debug_library()
+    assert dbg.fa_debug_arm(3, 0, 0, 0) == -8
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_LOSE_K_ARRIVAL, -1, 0, 0) == -2
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_LOSE_K_ARRIVAL, 0, -1, 0) == -2
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_SHRINK_OUTPUT, 5, 0, 1000001) == -2
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_SHRINK_OUTPUT, 5, 0, 1000) == 0
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_NONE, 0, 0, 0) == 0  # disarm
+    # no device status was read on this thread: nothing to report
+    assert dbg.fa_last_device_status() == 0
+    assert fa.fa_status_string(-12) != "unknown status"
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -1,0 +1,141 @@
+"""The debug build (include/fa_debug.h) on the GPU.
+
+- Its device index checks pass on valid requests, and its output is
+  bit-identical to the release build's.
+- A failed check is recorded (FA_ERR_CHECK, with the check's number) and its
+  store skipped.  The fault shrinks the extent that the checks use, so every
+  skipped store lay inside the real buffer.
+- A lost barrier arrival ends the launch with FA_ERR_TIMEOUT, not a hang,
+  and the context stays usable afterwards.
+"""
+import time
+
+import pytest
+import torch
+
+from online_softmax_fa_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+SENT_O, SENT_L = 1000.0, -1000.0  # outside any O or LSE these inputs can give
+FWD = 1 << 8  # kernel number of the forward (d 64, 128) in fa_last_device_status
+CHK_STORE_O = 6
+
+
+@pytest.fixture(scope="module")
+def libs():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from online_softmax_fa_gb300 import fa
+    from online_softmax_fa_gb300.build import build_library
+    build_library()
+    return fa, fa.load_library(), fa.load_debug_library()
+
+
+def _inputs(B, H, Hkv, N, d, seed):
+    q, k, v = make_qkv(B, H, N, d, seed=seed, H_kv=Hkv)
+    dev = torch.device("cuda")
+    return q.to(dev), k.to(dev), v.to(dev)
+
+
+def _outputs(q, o_offset=0):
+    """O (bf16, optionally starting o_offset elements into a larger buffer)
+    and LSE, filled with sentinels."""
+    B, H, N, d = q.shape
+    buf = torch.full((B * H * N * d + o_offset,), SENT_O, dtype=torch.bfloat16, device=q.device)
+    o = buf[o_offset:].view(B, H, N, d)
+    lse = torch.full((B, H, N), SENT_L, dtype=torch.float32, device=q.device)
+    return o, lse
+
+
+def _launch(lib, q, k, v, o, lse, causal):
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    stream = torch.cuda.current_stream().cuda_stream
+    scale = float(d) ** -0.5
+    rc = lib.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, Hkv, N, d, int(causal), scale, stream)
+    assert rc == 0
+    return lib.fa_device_error(stream)
+
+
+CLEAN_CASES = [
+    # B, H, H_kv, N, d, causal, O offset (8 elements: 16- but not 32-byte aligned)
+    (1, 2, 2, 300, 64, False, 0),
+    (1, 2, 2, 300, 64, True, 0),
+    (2, 3, 3, 1000, 128, True, 0),
+    (1, 4, 1, 777, 128, False, 0),
+    (1, 8, 2, 2048, 128, True, 0),
+    (1, 1, 1, 1, 128, True, 0),
+    (1, 2, 2, 129, 64, True, 8),
+    (2, 2, 2, 640, 128, False, 8),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,off", CLEAN_CASES)
+def test_checks_pass_and_match_release(libs, B, H, Hkv, N, d, causal, off):
+    fa, rel, dbg = libs
+    q, k, v = _inputs(B, H, Hkv, N, d, seed=40 + N)
+    o_r, l_r = _outputs(q, off)
+    o_d, l_d = _outputs(q, off)
+    assert _launch(rel, q, k, v, o_r, l_r, causal) == 0
+    assert _launch(dbg, q, k, v, o_d, l_d, causal) == 0
+    assert dbg.fa_last_device_status() == 0
+    assert torch.equal(o_r, o_d) and torch.equal(l_r, l_d)
+    assert not (o_d == SENT_O).any()  # every row was written
+
+
+def test_failed_store_check_is_recorded_and_skipped(libs):
+    fa, rel, dbg = libs
+    B, H, N, d = 1, 2, 300, 64
+    q, k, v = _inputs(B, H, H, N, d, seed=7)
+    o_r, l_r = _outputs(q)
+    assert _launch(rel, q, k, v, o_r, l_r, False) == 0
+    rows = B * H * N
+    # the checks take the output to end one row early: the last row's stores
+    # fail their check and are skipped
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_SHRINK_OUTPUT, rows - 1, 0, 20000) == 0
+    o, lse = _outputs(q)
+    assert _launch(dbg, q, k, v, o, lse, False) == fa.FA_ERR_CHECK
+    assert dbg.fa_last_device_status() == FWD | 0x80 | CHK_STORE_O
+    assert (o[0, 1, N - 1] == SENT_O).all() and lse[0, 1, N - 1] == SENT_L
+    # every other row holds the release result, or the sentinel where the
+    # aborted CTA stopped early
+    o_rows, r_rows = o.reshape(rows, d)[:-1], o_r.reshape(rows, d)[:-1]
+    written = ~(o_rows == SENT_O).all(dim=1)
+    assert torch.equal(o_rows[written], r_rows[written])
+    # an extent of zero rows: no store at all
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_SHRINK_OUTPUT, 0, 0, 20000) == 0
+    o, lse = _outputs(q)
+    assert _launch(dbg, q, k, v, o, lse, False) == fa.FA_ERR_CHECK
+    assert (o == SENT_O).all() and (lse == SENT_L).all()
+    # the fault was one-shot: the next launch is clean again
+    o, lse = _outputs(q)
+    assert _launch(dbg, q, k, v, o, lse, False) == 0
+    assert torch.equal(o, o_r) and torch.equal(lse, l_r)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_lost_arrival_times_out_and_context_survives(libs, causal):
+    fa, rel, dbg = libs
+    B, H, N, d = 1, 2, 1024, 128
+    q, k, v = _inputs(B, H, H, N, d, seed=9)
+    o_r, l_r = _outputs(q)
+    assert _launch(rel, q, k, v, o_r, l_r, causal) == 0
+    # work item 0 (the first CTA's own, 8 key tiles long in both orders)
+    # loses the arrival of its key tile 1; every wait is limited to 20 ms
+    assert dbg.fa_debug_arm(fa.FA_DEBUG_LOSE_K_ARRIVAL, 0, 1, 20000) == 0
+    o, lse = _outputs(q)
+    t0 = time.monotonic()
+    assert _launch(dbg, q, k, v, o, lse, causal) == fa.FA_ERR_TIMEOUT
+    assert time.monotonic() - t0 < 10.0
+    st = dbg.fa_last_device_status()
+    assert st >> 8 == 1 and 1 <= (st & 0xFF) <= 13, hex(st)  # a forward wait ran out
+    assert dbg.fa_device_error(None) == 0  # cleared
+    # the context is usable: a clean launch of both builds matches
+    o, lse = _outputs(q)
+    assert _launch(dbg, q, k, v, o, lse, causal) == 0
+    assert torch.equal(o, o_r) and torch.equal(lse, l_r)
+    o2, l2 = _outputs(q)
+    assert _launch(rel, q, k, v, o2, l2, causal) == 0
+    assert torch.equal(o2, o_r)

@@ -297,7 +297,9 @@ def test_bounded_wait_expires_with_status(fa):
     """A wait nothing signals ends with FA_ERR_TIMEOUT, not a hang, and the
     context stays usable afterwards."""
     assert fa.fa_selftest_bounded_wait(20000) == fa.FA_ERR_TIMEOUT
+    assert fa.fa_last_device_status() == (1 << 8) | 0x7F  # forward word, the test's wait
     assert fa.fa_device_error() == 0  # the status word was cleared
+    assert fa.fa_last_device_status() == 0
     q, k, v = make_qkv(1, 1, 256, 64, seed=1)
     o, lse = run(fa, q, k, v, False, 0.125)
     O_ref, L_ref = oracle.attention_fwd(q, k, v, scale=0.125)
