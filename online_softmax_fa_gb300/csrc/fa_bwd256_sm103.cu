@@ -13,22 +13,25 @@
 // share an SM with the S^T / dP^T tiles, and 128-row K, V, Q, dO tiles are
 // 64 KB each in shared memory.  So:
 //   * dkdv: two CTAs per 128-key block, one per 128-column slice of dV and
-//     dK (S^T and dP^T need all of d, so both CTAs compute them).  K_j and
-//     V_j stay in shared memory (128 KB); the query rows stream in 64-row
-//     halves (Q and dO, 64 KB, one stage).  Per half: S^T = K_j Q_h^T and
-//     dP^T = V_j dO_h^T (16 K-steps each, N = 64), P^T and dS^T by eight
-//     elementwise warps (thread = key row, 32 query columns per warp), then
-//     dV_s += P^T dO_h[:, s] and dK_s += dS^T Q_h[:, s] (N = 128, A from
-//     TMEM).  TMEM: S^T [0, 64), dP^T [64, 128), dV_s [256, 384), dK_s
-//     [384, 512); P^T and dS^T as bf16 pairs over S^T's columns.
-//   * dq: one CTA per 128-query block; Q_i and dO_i stay (128 KB), the keys
-//     stream in 64-row halves (K and V, 64 KB, one stage).  Per half: S and
-//     dP (N = 64), dS (thread = query row), then dQ += dS K_h as one
-//     M128 x N256 MMA per 16 keys.  TMEM: S [0, 64), dP [64, 128), dQ
-//     [256, 512).
-// One shared-memory stage means a half's loads wait for the previous half's
-// last MMA; the kernels are correct and deterministic (no atomics, fixed
-// order), not fast.  Causal: blocks above the diagonal are skipped, the
+//     dK (S^T and dP^T need all of d, so both CTAs compute them).  V_j stays
+//     in shared memory (64 KB) and K_j in TMEM columns [128, 256) (copied
+//     there once, with tcgen05.cp, through a shared-memory stage), where the
+//     S^T MMAs read it as their A operand; the query rows stream in 64-row
+//     halves (Q and dO, 64 KB) through two stages, so a half's loads overlap
+//     the previous half's MMAs.  Per half: S^T = K_j Q_h^T and dP^T = V_j
+//     dO_h^T (16 K-steps each, N = 64), P^T and dS^T by eight elementwise
+//     warps (thread = key row, 32 query columns per warp), then dV_s +=
+//     P^T dO_h[:, s] and dK_s += dS^T Q_h[:, s] (N = 128, A from TMEM).
+//     TMEM: S^T [0, 64), dP^T [64, 128), K_j [128, 256), dV_s [256, 384),
+//     dK_s [384, 512); P^T and dS^T as bf16 pairs over S^T's columns.
+//   * dq: one CTA per 128-query block; dO_i stays in shared memory and Q_i
+//     in TMEM [128, 256) the same way; the keys stream in 64-row halves (K
+//     and V, 64 KB) through two stages.  Per half: S and dP (N = 64), dS
+//     (thread = query row), then dQ += dS K_h as one M128 x N256 MMA per 16
+//     keys.  TMEM: S [0, 64), dP [64, 128), Q_i [128, 256), dQ [256, 512).
+// TMEM holds one S^T / dP^T pair, so a half's MMAs wait for the elementwise
+// step of the previous half.  The kernels are deterministic (no atomics,
+// fixed order).  Causal: blocks above the diagonal are skipped, the
 // diagonal block and a ragged last block masked per element.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -57,17 +60,20 @@ constexpr int kEwWarps = 8;
 constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr uint32_t kRegsEw = 216, kRegsCtl = 72;  // 128 x (216 + 216 + 72) = 384 x 168
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmS = 0, kTmP = 64, kTmAcc = 256;
+constexpr uint32_t kTmS = 0, kTmP = 64, kTmOp = 128, kTmAcc = 256;  // kTmOp: K_j or Q_i
 constexpr float kLog2e = 1.4426950408889634f;
 
-// shared memory: the resident tiles A (K_j or Q_i) and B (V_j or dO_i),
-// the streamed half-tiles C (Q_h or K_h) and E (dO_h or V_h), the half's
-// statistics (dkdv), barriers
-constexpr int kOffA = 0, kOffB = kTile, kOffC = 2 * kTile, kOffE = 2 * kTile + kHTile;
-constexpr int kOffRows = 2 * kTile + 2 * kHTile;  // dkdv: -LSE2[64], -D[64]
-constexpr int kOffBar = kOffRows + 2 * kHalf * 4;
-// once, full, empty, s_full, p_full, o_full
-constexpr int kNumBars = 6;
+// shared memory: the resident tile A (V_j or dO_i); two stages, each the
+// streamed half-tiles C (Q_h or K_h) and E (dO_h or V_h); the stages' row
+// statistics (dkdv); barriers.  Stage 1 first holds the tile that goes to
+// TMEM (K_j or Q_i, 64 KB = one stage).
+constexpr int kStages = 2;
+constexpr int kStage = 2 * kHTile;
+constexpr int kOffA = 0, kOffStage = kTile;
+constexpr int kOffRows = kOffStage + kStages * kStage;  // dkdv: per stage -LSE2[64], -D[64]
+constexpr int kOffBar = kOffRows + kStages * 2 * kHalf * 4;
+// once, full[2], empty[2], s_full, p_full, o_full
+constexpr int kNumBars = 8;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -91,11 +97,13 @@ struct Params {
 };
 
 struct View {
-    uint8_t *a, *b, *c, *e;
-    float *rows;
-    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;
+    uint8_t *a, *stage;  // stage s at stage + s * kStage: C, then E
+    float *rows;         // stage s's statistics at rows + s * 2 * kHalf
+    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;  // full, empty: [2]
     uint32_t *tmem_slot;
     volatile int *abort_flag;
+    __device__ uint8_t *c(int s) const { return stage + s * kStage; }
+    __device__ uint8_t *e(int s) const { return stage + s * kStage + kHTile; }
 };
 
 __device__ __forceinline__ View view() {
@@ -104,17 +112,15 @@ __device__ __forceinline__ View view() {
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     View v;
     v.a = smem + kOffA;
-    v.b = smem + kOffB;
-    v.c = smem + kOffC;
-    v.e = smem + kOffE;
+    v.stage = smem + kOffStage;
     v.rows = reinterpret_cast<float *>(smem + kOffRows);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     v.once = bar;
     v.full = bar + 1;
-    v.empty = bar + 2;
-    v.s_full = bar + 3;
-    v.p_full = bar + 4;
-    v.o_full = bar + 5;
+    v.empty = bar + 3;
+    v.s_full = bar + 5;
+    v.p_full = bar + 6;
+    v.o_full = bar + 7;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     return v;
@@ -160,6 +166,44 @@ __device__ __forceinline__ void mma_rows_k256(uint32_t d_tm, uint64_t da, uint64
         const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * kHBox + in) >> 4);
         mma_ss_elect(d_tm, da + oa, db + ob, kIdescSdp, kk > 0 ? 1u : 0u);
     }
+}
+
+// D[M128 x N64] = A[tmem, 128 x 256 bf16 at kTmOp] * B[64 rows x 256]^T, B
+// K-major in four 64-column swizzled chunks 8 KB apart.
+__device__ __forceinline__ void mma_tmem_rows_k256(uint32_t d_tm, uint32_t a_tm, uint64_t db) {
+#pragma unroll 4
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * kHBox + (kk & 3) * 32) >> 4);
+        mma_ts_elect(d_tm, a_tm + 8 * kk, db + ob, kIdescSdp, kk > 0 ? 1u : 0u);
+    }
+}
+
+// Copies a [128 x 256] bf16 tile (K-major, four 64-column swizzled chunks
+// 16 KB apart, descriptor da) into TMEM columns [a_tm, a_tm + 128) as an A
+// operand: K-step kk (16 elements) into columns a_tm + 8 kk.
+__device__ __forceinline__ void copy_tile_to_tmem(uint32_t a_tm, uint64_t da) {
+#pragma unroll 4
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+        tmem_cp_128x256b_elect(a_tm + 8 * kk, da + oa);
+    }
+}
+
+// The producer's wait before it loads half u into stage u & 1.  Stage 0
+// holds halves 0, 2, 4, ...; stage 1 first holds the tile copied into TMEM
+// (its release is the first completion of empty[1]), then halves 1, 3, ...
+__device__ __forceinline__ bool wait_stage_free(const View &v, int u, const WaitCtl &ctl) {
+    const int s = u & 1, use = u >> 1;
+    if (s == 0) return use == 0 || mbar_wait(&v.empty[0], (use - 1) & 1, ctl, kSiteEmpty);
+    return mbar_wait(&v.empty[1], use & 1, ctl, kSiteEmpty);
+}
+
+// Drain of the producer's copies on the way out: the resident tiles and the
+// last two halves issued (one per stage).
+__device__ __forceinline__ void drain_loads(const View &v, int issued, uint64_t limit_ns) {
+    mbar_wait_drain(v.once, 0, limit_ns);
+    for (int u = max(0, issued - kStages); u < issued; ++u)
+        mbar_wait_drain(&v.full[u & 1], (u >> 1) & 1, limit_ns);
 }
 
 // acc (+)= A[tmem, 128 x 64 bf16] * B[64 rows x N, MN-major], the A pairs
@@ -208,8 +252,10 @@ __device__ __forceinline__ void p_ds32(const uint32_t (&s)[32], const uint32_t (
 
 __device__ __forceinline__ void setup(const View &v) {
     mbar_init(v.once, 1);
-    mbar_init(v.full, 1);
-    mbar_init(v.empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(&v.full[s], 1);
+        mbar_init(&v.empty[s], 1);
+    }
     mbar_init(v.s_full, 1);
     mbar_init(v.p_full, kEwWarps);
     mbar_init(v.o_full, 1);
@@ -230,26 +276,25 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQh, const CUt
     const int n_u = 2 * p.group * n_q;
     const uint64_t pol = l2_policy_evict_last();
     mbar_arrive_expect_tx(v.once, 2 * kTile);
-    load_rows(v.a, kBox, tmK, v.once, jb * kBlk, bh, pol);
-    load_rows(v.b, kBox, tmV, v.once, jb * kBlk, bh, pol);
+    load_rows(v.a, kBox, tmV, v.once, jb * kBlk, bh, pol);         // V_j, resident
+    load_rows(v.c(1), kBox, tmK, v.once, jb * kBlk, bh, pol);      // K_j, for TMEM
     int issued = 0;
-    bool ok = true;
-    for (int u = 0; u < n_u && ok; ++u) {
-        if (u > 0) ok = mbar_wait(v.empty, (u - 1) & 1, ctl, kSiteEmpty);
-        if (!ok) break;
+    for (int u = 0; u < n_u; ++u) {
+        if (!wait_stage_free(v, u, ctl)) break;
+        const int s = u & 1;
         const int t = u >> 1, g = t / n_q;
         const int qr = (i0 + t - g * n_q) * kBlk + (u & 1) * kHalf;  // the half's first query
         const int bq = q_head(p, bh, g);
         const size_t prow = static_cast<size_t>(bq) * p.n_blocks * kBlk + qr;
-        mbar_arrive_expect_tx(v.full, 2 * kHTile + 2 * kHalf * 4);
-        load_rows(v.c, kHBox, tmQh, v.full, qr, bq, pol);
-        load_rows(v.e, kHBox, tmdOh, v.full, qr, bq, pol);
-        bulk_load(v.rows, p.lse2 + prow, kHalf * 4, v.full, pol);
-        bulk_load(v.rows + kHalf, p.dd + prow, kHalf * 4, v.full, pol);
+        float *rows = v.rows + s * 2 * kHalf;
+        mbar_arrive_expect_tx(&v.full[s], 2 * kHTile + 2 * kHalf * 4);
+        load_rows(v.c(s), kHBox, tmQh, &v.full[s], qr, bq, pol);
+        load_rows(v.e(s), kHBox, tmdOh, &v.full[s], qr, bq, pol);
+        bulk_load(rows, p.lse2 + prow, kHalf * 4, &v.full[s], pol);
+        bulk_load(rows + kHalf, p.dd + prow, kHalf * 4, &v.full[s], pol);
         ++issued;
     }
-    mbar_wait_drain(v.once, 0, p.limit_ns);
-    if (issued > 0) mbar_wait_drain(v.full, (issued - 1) & 1, p.limit_ns);
+    drain_loads(v, issued, p.limit_ns);
 }
 
 template <bool CAUSAL>
@@ -261,22 +306,30 @@ __device__ __forceinline__ void dkdv_mma(const Params &p, int jb, int slice) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t dK = sdesc_sw128(smem_u32(v.a), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_u32(v.b), 16, 1024);
-    const uint64_t dQh = sdesc_sw128(smem_u32(v.c), 16, 1024);
-    const uint64_t ddOh = sdesc_sw128(smem_u32(v.e), 16, 1024);
-    // the slice's two chunks of Q_h / dO_h as MN-major B operands (N = 128:
-    // chunks 2s and 2s + 1, kHBox apart)
-    const uint64_t dQs = sdesc_sw128(smem_u32(v.c + 2 * slice * kHBox), kHBox, 1024);
-    const uint64_t ddOs = sdesc_sw128(smem_u32(v.e + 2 * slice * kHBox), kHBox, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(v.a), 16, 1024);
+    // K_j, staged in stage 1, into TMEM; its copies complete (and stage 1 is
+    // free) at the first completion of empty[1]
     bool ok = wait(v.once, 0, kSiteOnce);
+    if (ok) {
+        tc_fence_after();
+        copy_tile_to_tmem(tmem + kTmOp, sdesc_sw128(smem_u32(v.c(1)), 16, 1024));
+        mma_commit_elect(&v.empty[1]);
+        ok = wait(&v.empty[1], 0, kSiteEmpty);
+    }
     for (int u = 0; u < n_u && ok; ++u) {
-        ok = wait(v.full, u & 1, kSiteFull);
+        const int s = u & 1;
+        ok = wait(&v.full[s], (u >> 1) & 1, kSiteFull);
         if (!ok) break;
         tc_fence_after();
+        const uint64_t dQh = sdesc_sw128(smem_u32(v.c(s)), 16, 1024);
+        const uint64_t ddOh = sdesc_sw128(smem_u32(v.e(s)), 16, 1024);
+        // the slice's two chunks of Q_h / dO_h as MN-major B operands (N =
+        // 128: chunks 2 slice and 2 slice + 1, kHBox apart)
+        const uint64_t dQs = sdesc_sw128(smem_u32(v.c(s) + 2 * slice * kHBox), kHBox, 1024);
+        const uint64_t ddOs = sdesc_sw128(smem_u32(v.e(s) + 2 * slice * kHBox), kHBox, 1024);
         // S^T and dP^T of this half (the previous half's dV / dK, which read
         // the same TMEM columns, were issued before by this thread)
-        mma_rows_k256(tmem + kTmS, dK, dQh);
+        mma_tmem_rows_k256(tmem + kTmS, tmem + kTmOp, dQh);
         mma_rows_k256(tmem + kTmP, dV, ddOh);
         mma_commit_elect(v.s_full);
         ok = wait(v.p_full, u & 1, kSiteP);
@@ -284,7 +337,7 @@ __device__ __forceinline__ void dkdv_mma(const Params &p, int jb, int slice) {
         tc_fence_after();
         mma_tmem_k64(tmem + kTmAcc, tmem + kTmS, ddOs, kIdescSlice, u > 0);             // dV_s
         mma_tmem_k64(tmem + kTmAcc + 128, tmem + kTmS + 16, dQs, kIdescSlice, u > 0);  // dK_s
-        mma_commit_elect(v.empty);  // the stage is read
+        mma_commit_elect(&v.empty[s]);  // the stage is read
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
@@ -305,7 +358,8 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        ok = mbar_wait(v.full, u & 1, ctl, kSiteFull);  // the half's statistics landed
+        const float *rows = v.rows + (u & 1) * 2 * kHalf;
+        ok = mbar_wait(&v.full[u & 1], (u >> 1) & 1, ctl, kSiteFull);  // the half's statistics
         if (ok) ok = mbar_wait(v.s_full, u & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
@@ -319,7 +373,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
         uint32_t sv[32], dv[32], pp[16], pds[16];
         const uint32_t ts = tmem + lb + kTmS + 32 * c, tp = tmem + lb + kTmP + 32 * c;
         tmem_ld32x2(ts, tp, sv, dv);
-        p_ds32(sv, dv, v.rows + 32 * c, v.rows + kHalf + 32 * c, true, 0.f, 0.f, p.scale_log2,
+        p_ds32(sv, dv, rows + 32 * c, rows + kHalf + 32 * c, true, 0.f, 0.f, p.scale_log2,
                masked, lim_lo, lim_hi, 32 * c, pp, pds);
         tmem_st16(ts, pp);         // P^T over the first 16 of this warp's columns
         tmem_st16(ts + 16, pds);   // dS^T over the next 16
@@ -410,20 +464,18 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     const int bk = kv_head(p, bh);
     const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(v.once, 2 * kTile);
-    load_rows(v.a, kBox, tmQ, v.once, ib * kBlk, bh, pol_q);
-    load_rows(v.b, kBox, tmdO, v.once, ib * kBlk, bh, pol_q);
+    load_rows(v.a, kBox, tmdO, v.once, ib * kBlk, bh, pol_q);    // dO_i, resident
+    load_rows(v.c(1), kBox, tmQ, v.once, ib * kBlk, bh, pol_q);  // Q_i, for TMEM
     int issued = 0;
-    bool ok = true;
-    for (int u = 0; u < n_u && ok; ++u) {
-        if (u > 0) ok = mbar_wait(v.empty, (u - 1) & 1, ctl, kSiteEmpty);
-        if (!ok) break;
-        mbar_arrive_expect_tx(v.full, 2 * kHTile);
-        load_rows(v.c, kHBox, tmKh, v.full, u * kHalf, bk, pol_kv);
-        load_rows(v.e, kHBox, tmVh, v.full, u * kHalf, bk, pol_kv);
+    for (int u = 0; u < n_u; ++u) {
+        if (!wait_stage_free(v, u, ctl)) break;
+        const int s = u & 1;
+        mbar_arrive_expect_tx(&v.full[s], 2 * kHTile);
+        load_rows(v.c(s), kHBox, tmKh, &v.full[s], u * kHalf, bk, pol_kv);
+        load_rows(v.e(s), kHBox, tmVh, &v.full[s], u * kHalf, bk, pol_kv);
         ++issued;
     }
-    mbar_wait_drain(v.once, 0, p.limit_ns);
-    if (issued > 0) mbar_wait_drain(v.full, (issued - 1) & 1, p.limit_ns);
+    drain_loads(v, issued, p.limit_ns);
 }
 
 template <bool CAUSAL>
@@ -435,24 +487,31 @@ __device__ __forceinline__ void dq_mma(const Params &p, int ib) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t dQ = sdesc_sw128(smem_u32(v.a), 16, 1024);
-    const uint64_t ddO = sdesc_sw128(smem_u32(v.b), 16, 1024);
-    const uint64_t dKh = sdesc_sw128(smem_u32(v.c), 16, 1024);
-    const uint64_t dVh = sdesc_sw128(smem_u32(v.e), 16, 1024);
-    const uint64_t dKmn = sdesc_sw128(smem_u32(v.c), kHBox, 1024);  // K_h as MN-major B, N = 256
+    const uint64_t ddO = sdesc_sw128(smem_u32(v.a), 16, 1024);
+    // Q_i, staged in stage 1, into TMEM (as in the dK / dV kernel)
     bool ok = wait(v.once, 0, kSiteOnce);
+    if (ok) {
+        tc_fence_after();
+        copy_tile_to_tmem(tmem + kTmOp, sdesc_sw128(smem_u32(v.c(1)), 16, 1024));
+        mma_commit_elect(&v.empty[1]);
+        ok = wait(&v.empty[1], 0, kSiteEmpty);
+    }
     for (int u = 0; u < n_u && ok; ++u) {
-        ok = wait(v.full, u & 1, kSiteFull);
+        const int s = u & 1;
+        ok = wait(&v.full[s], (u >> 1) & 1, kSiteFull);
         if (!ok) break;
         tc_fence_after();
-        mma_rows_k256(tmem + kTmS, dQ, dKh);   // S = Q K_h^T
-        mma_rows_k256(tmem + kTmP, ddO, dVh);  // dP = dO V_h^T
+        const uint64_t dKh = sdesc_sw128(smem_u32(v.c(s)), 16, 1024);
+        const uint64_t dVh = sdesc_sw128(smem_u32(v.e(s)), 16, 1024);
+        const uint64_t dKmn = sdesc_sw128(smem_u32(v.c(s)), kHBox, 1024);  // MN-major B, N = 256
+        mma_tmem_rows_k256(tmem + kTmS, tmem + kTmOp, dKh);  // S = Q K_h^T
+        mma_rows_k256(tmem + kTmP, ddO, dVh);                // dP = dO V_h^T
         mma_commit_elect(v.s_full);
         ok = wait(v.p_full, u & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
         mma_tmem_k64(tmem + kTmAcc, tmem + kTmS, dKmn, kIdescDq, u > 0);  // dQ += dS K_h
-        mma_commit_elect(v.empty);
+        mma_commit_elect(&v.empty[s]);
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);

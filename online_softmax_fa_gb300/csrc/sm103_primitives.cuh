@@ -263,6 +263,20 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// Copy of one M128 x K16 operand slice (128 rows x 32 bytes) from a 128-byte
+// swizzled, K-major shared-memory tile (descriptor `sdesc`) into 8 TMEM
+// columns at `taddr`, laid out as an MMA reads an A operand from TMEM (lane
+// r, column c = elements 2c, 2c + 1 of row r).  Asynchronous: a later
+// tcgen05.commit by the same thread tracks its completion.
+__device__ __forceinline__ void tmem_cp_128x256b_elect(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
