@@ -41,6 +41,7 @@
 
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
+#include "bwd_elementwise.cuh"
 
 namespace fa {
 
@@ -225,31 +226,6 @@ __device__ __forceinline__ void load_rows(uint8_t *dst, int chunk_bytes, const C
     for (int c = 0; c < 4; ++c) tma_load_3d(dst + c * chunk_bytes, m, bar, 64 * c, row, bh, pol);
 }
 
-// p = 2^(s*c + nl2), ds = p * (dp + nd) for 32 columns, column col0 + e kept
-// iff lim_lo <= col0 + e < lim_hi (p = 0 elsewhere); per-column statistics
-// (col_stats) or one per row.
-__device__ __forceinline__ void p_ds32(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                       const float *nl2, const float *nd, bool col_stats,
-                                       float my_nl2, float my_nd, float cs, bool masked,
-                                       int lim_lo, int lim_hi, int col0, uint32_t (&pp)[16],
-                                       uint32_t (&pds)[16]) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-        float pv[2], dv[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int e = 2 * t + u;
-            const float l2 = col_stats ? nl2[e] : my_nl2;
-            const float d = col_stats ? nd[e] : my_nd;
-            const bool keep = !masked || (col0 + e >= lim_lo && col0 + e < lim_hi);
-            pv[u] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), cs, l2)) : 0.f;
-            dv[u] = pv[u] * (__uint_as_float(dp[e]) + d);
-        }
-        pp[t] = pack_bf16x2(pv[0], pv[1]);
-        pds[t] = pack_bf16x2(dv[0], dv[1]);
-    }
-}
-
 __device__ __forceinline__ void setup(const View &v) {
     mbar_init(v.once, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -358,9 +334,18 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        const float *rows = v.rows + (u & 1) * 2 * kHalf;
+        const float *rows = v.rows + (u & 1) * 2 * kHalf + 32 * c;
         ok = mbar_wait(&v.full[u & 1], (u >> 1) & 1, ctl, kSiteFull);  // the half's statistics
-        if (ok) ok = mbar_wait(v.s_full, u & 1, ctl, kSiteS);
+        if (!ok) break;
+        // this warp's 32 columns' statistics into registers before S^T is
+        // ready (read during the math, they would wait on shared memory)
+        float4 l4[8], d4[8];
+#pragma unroll
+        for (int t4 = 0; t4 < 8; ++t4) {
+            l4[t4] = *reinterpret_cast<const float4 *>(rows + 4 * t4);
+            d4[t4] = *reinterpret_cast<const float4 *>(rows + kHalf + 4 * t4);
+        }
+        ok = mbar_wait(v.s_full, u & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
         const int t = u >> 1;
@@ -373,8 +358,11 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
         uint32_t sv[32], dv[32], pp[16], pds[16];
         const uint32_t ts = tmem + lb + kTmS + 32 * c, tp = tmem + lb + kTmP + 32 * c;
         tmem_ld32x2(ts, tp, sv, dv);
-        p_ds32(sv, dv, rows + 32 * c, rows + kHalf + 32 * c, true, 0.f, 0.f, p.scale_log2,
-               masked, lim_lo, lim_hi, 32 * c, pp, pds);
+        if (masked)
+            p_ds_masked(sv, dv, rows, rows + kHalf, true, 0.f, 0.f, p.scale_log2, lim_lo, lim_hi,
+                        32 * c, pp, pds);
+        else
+            p_ds_fast_reg(sv, dv, l4, d4, p.scale_log2, pp, pds);
         tmem_st16(ts, pp);         // P^T over the first 16 of this warp's columns
         tmem_st16(ts + 16, pds);   // dS^T over the next 16
         tmem_wait_st();
@@ -542,8 +530,11 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
         uint32_t sv[32], dv[32], pp[16], pds[16];
         const uint32_t ts = tmem + lb + kTmS + 32 * c, tp = tmem + lb + kTmP + 32 * c;
         tmem_ld32x2(ts, tp, sv, dv);
-        p_ds32(sv, dv, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, masked, 0, lim_hi,
-               32 * c, pp, pds);
+        if (masked)
+            p_ds_masked(sv, dv, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, 0, lim_hi,
+                        32 * c, pp, pds);
+        else
+            p_ds_fast(sv, dv, nullptr, nullptr, false, my_nl2, my_nd, p.scale_log2, pp, pds);
         tmem_st16(ts, pds);  // dS over the first 16 of this warp's columns
         tmem_wait_st();
         tc_fence_before();
