@@ -105,4 +105,43 @@ __device__ __forceinline__ void p_ds_masked(const uint32_t (&s)[32], const uint3
     }
 }
 
+
+// P alone (the d = 256 dV kernel role, which needs no dS): p = 2^(s*c -
+// lse2) for 32 consecutive columns as packed bf16 pairs, the columns'
+// negated statistics nl2 in registers; masked, column col0 + e is kept iff
+// lim_lo <= col0 + e < lim_hi (p = 0 elsewhere).
+__device__ __forceinline__ float f4_at(const float4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void p_only_reg(const uint32_t (&s)[32], const float4 (&l4)[8],
+                                           float cs, bool masked, int lim_lo, int lim_hi,
+                                           int col0, uint32_t (&pp)[16]) {
+    if (!masked) {
+        const uint64_t cs2 = f2_pack(cs, cs);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const int e = 2 * t;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), cs2,
+                             f2_pack(f4_at(l4[e >> 2], e & 3), f4_at(l4[e >> 2], (e & 3) + 1))),
+                      x0, x1);
+            pp[t] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = 2 * t + u, col = col0 + e;
+                const bool keep = col >= lim_lo && col < lim_hi;
+                pv[u] = keep ? ex2_approx(fmaf(__uint_as_float(s[e]), cs, f4_at(l4[e >> 2], e & 3)))
+                             : 0.f;
+            }
+            pp[t] = pack_bf16x2(pv[0], pv[1]);
+        }
+    }
+}
+
 }  // namespace fa

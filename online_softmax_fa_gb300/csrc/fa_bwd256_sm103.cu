@@ -12,18 +12,21 @@
 // 256 is half of TMEM, so dV and dK of one key block (512 columns) cannot
 // share an SM with the S^T / dP^T tiles, and 128-row K, V, Q, dO tiles are
 // 64 KB each in shared memory.  So:
-//   * dkdv: two CTAs per 128-key block, one per 128-column slice of dV and
-//     dK (S^T and dP^T need all of d, so both CTAs compute them).  V_j stays
-//     in shared memory (64 KB) and K_j in TMEM columns [128, 256) (copied
-//     there once, with tcgen05.cp, through a shared-memory stage), where the
-//     S^T MMAs read it as their A operand; the query rows stream in 64-row
-//     halves (Q and dO, 64 KB) through two stages, so a half's loads overlap
-//     the previous half's MMAs.  Per half: S^T = K_j Q_h^T and dP^T = V_j
-//     dO_h^T (16 K-steps each, N = 64), P^T and dS^T by eight elementwise
-//     warps (thread = key row, 32 query columns per warp), then dV_s +=
-//     P^T dO_h[:, s] and dK_s += dS^T Q_h[:, s] (N = 128, A from TMEM).
-//     TMEM: S^T [0, 64), dP^T [64, 128), K_j [128, 256), dV_s [256, 384),
-//     dK_s [384, 512); P^T and dS^T as bf16 pairs over S^T's columns.
+//   * dkdv: two CTAs per 128-key block, one for dV and one for dK, each
+//     with its 256-column accumulator in TMEM [256, 512) (S^T needs all of
+//     d, so both compute it).  Both hold K_j in TMEM columns [128, 256)
+//     (copied there once, with tcgen05.cp, through a shared-memory stage),
+//     where the S^T MMAs read it as their A operand, and stream the query
+//     rows in 64-row halves (Q and dO, 64 KB) through shared-memory stages,
+//     so a half's loads overlap the previous half's MMAs.  Per half: S^T =
+//     K_j Q_h^T (16 K-steps, N = 64); the dV CTA forms P^T (thread = key
+//     row, 32 query columns per warp) and adds P^T dO_h (N = 256, A from
+//     TMEM), with S^T double-buffered in [0, 64) and [64, 128) so the next
+//     half's S^T overlaps the elementwise step, over three stages; the dK
+//     CTA also computes dP^T = V_j dO_h^T (V_j resident in shared memory),
+//     forms dS^T and adds dS^T Q_h, with one S^T / dP^T pair ([0, 64),
+//     [64, 128)) over two stages.  P^T and dS^T are bf16 pairs written over
+//     S^T's columns.
 //   * dq: one CTA per 128-query block; dO_i stays in shared memory and Q_i
 //     in TMEM [128, 256) the same way; the keys stream in 64-row halves (K
 //     and V, 64 KB) through two stages.  Per half: S and dP (N = 64), dS
@@ -64,23 +67,23 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmS = 0, kTmP = 64, kTmOp = 128, kTmAcc = 256;  // kTmOp: K_j or Q_i
 constexpr float kLog2e = 1.4426950408889634f;
 
-// shared memory: the resident tile A (V_j or dO_i); two stages, each the
-// streamed half-tiles C (Q_h or K_h) and E (dO_h or V_h); the stages' row
-// statistics (dkdv); barriers.  Stage 1 first holds the tile that goes to
-// TMEM (K_j or Q_i, 64 KB = one stage).
-constexpr int kStages = 2;
-constexpr int kStage = 2 * kHTile;
-constexpr int kOffA = 0, kOffStage = kTile;
-constexpr int kOffRows = kOffStage + kStages * kStage;  // dkdv: per stage -LSE2[64], -D[64]
-constexpr int kOffBar = kOffRows + kStages * 2 * kHalf * 4;
-// once, full[2], empty[2], s_full, p_full, o_full
-constexpr int kNumBars = 8;
+// shared memory: three 64 KB regions R0-R2, the row statistics of each
+// region (dkdv: -LSE2[64], -D[64]), barriers.  A stage is a region holding
+// the streamed half-tiles C (Q_h or K_h) and E (dO_h or V_h).  The dK CTA
+// and dQ keep their resident tile (V_j or dO_i) in R0 and stream through
+// R1, R2; the dV CTA streams through all three.  R2 first holds the tile
+// that goes to TMEM (K_j or Q_i), then serves as the last stage.
+constexpr int kRegion = 2 * kHTile;  // 64 KB = one [128 x 256] bf16 tile
+constexpr int kRegions = 3;
+constexpr int kOffRows = kRegions * kRegion;
+constexpr int kOffBar = kOffRows + kRegions * 2 * kHalf * 4;
+// once, full[3], empty[3], s_full[2], p_full[2], o_full
+constexpr int kNumBars = 12;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescSdp = idesc_bf16_f32(kBlk, kHalf, false);      // M128 N64, K-major
-constexpr uint32_t kIdescSlice = idesc_bf16_f32(kBlk, 128, true);       // M128 N128, B MN-major
 constexpr uint32_t kIdescDq = idesc_bf16_f32(kBlk, kD, true);           // M128 N256, B MN-major
 
 enum : int { kSiteOnce = 0x51, kSiteFull, kSiteEmpty, kSiteS, kSiteP, kSiteO };
@@ -98,13 +101,16 @@ struct Params {
 };
 
 struct View {
-    uint8_t *a, *stage;  // stage s at stage + s * kStage: C, then E
-    float *rows;         // stage s's statistics at rows + s * 2 * kHalf
-    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;  // full, empty: [2]
+    uint8_t *base;     // region r at base + r * kRegion: C, then E
+    float *rows_base;  // region r's statistics at rows_base + r * 2 * kHalf
+    // full, empty: [3], per stage; s_full, p_full: [2], per S^T buffer (the
+    // dV CTA double-buffers S^T; the others use [0])
+    uint64_t *once, *full, *empty, *s_full, *p_full, *o_full;
     uint32_t *tmem_slot;
     volatile int *abort_flag;
-    __device__ uint8_t *c(int s) const { return stage + s * kStage; }
-    __device__ uint8_t *e(int s) const { return stage + s * kStage + kHTile; }
+    __device__ uint8_t *c(int r) const { return base + r * kRegion; }
+    __device__ uint8_t *e(int r) const { return base + r * kRegion + kHTile; }
+    __device__ float *rows(int r) const { return rows_base + r * 2 * kHalf; }
 };
 
 __device__ __forceinline__ View view() {
@@ -112,23 +118,22 @@ __device__ __forceinline__ View view() {
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     View v;
-    v.a = smem + kOffA;
-    v.stage = smem + kOffStage;
-    v.rows = reinterpret_cast<float *>(smem + kOffRows);
+    v.base = smem;
+    v.rows_base = reinterpret_cast<float *>(smem + kOffRows);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
     v.once = bar;
     v.full = bar + 1;
-    v.empty = bar + 3;
-    v.s_full = bar + 5;
-    v.p_full = bar + 6;
-    v.o_full = bar + 7;
+    v.empty = bar + 4;
+    v.s_full = bar + 7;
+    v.p_full = bar + 9;
+    v.o_full = bar + 11;
     v.tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     v.abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     return v;
 }
 
 // CTA -> (head row, block), causal in cost order within head groups (the
-// d <= 128 backward's order); dkdv CTAs come in pairs, one per d-slice.
+// d <= 128 backward's order); dkdv CTAs come in pairs, dV's and dK's.
 template <bool CAUSAL, bool KEY_BLOCKS>
 __device__ __forceinline__ void block_of(const Params &p, int x, int &bh, int &blk) {
     if (CAUSAL) {
@@ -190,21 +195,43 @@ __device__ __forceinline__ void copy_tile_to_tmem(uint32_t a_tm, uint64_t da) {
     }
 }
 
-// The producer's wait before it loads half u into stage u & 1.  Stage 0
-// holds halves 0, 2, 4, ...; stage 1 first holds the tile copied into TMEM
-// (its release is the first completion of empty[1]), then halves 1, 3, ...
+// A ring of STAGES stages over the last STAGES regions: half u goes to
+// stage u % STAGES = region (3 - STAGES) + u % STAGES, and is that stage's
+// (u / STAGES)-th half.
+template <int STAGES>
+__device__ __forceinline__ int region_of(int u) {
+    return (kRegions - STAGES) + u % STAGES;
+}
+
+// The producer's wait before it loads half u.  A stage below the last one
+// is free for its k-th half once its (k-1)-th half is released; the last
+// stage (R2) first holds the tile copied into TMEM, whose release is the
+// first completion of its empty barrier.
+template <int STAGES>
 __device__ __forceinline__ bool wait_stage_free(const View &v, int u, const WaitCtl &ctl) {
-    const int s = u & 1, use = u >> 1;
-    if (s == 0) return use == 0 || mbar_wait(&v.empty[0], (use - 1) & 1, ctl, kSiteEmpty);
-    return mbar_wait(&v.empty[1], use & 1, ctl, kSiteEmpty);
+    const int s = u % STAGES, use = u / STAGES;
+    const int done = (s == STAGES - 1) ? use : use - 1;  // 0-based completion of empty[s]
+    return done < 0 || mbar_wait(&v.empty[s], done & 1, ctl, kSiteEmpty);
 }
 
 // Drain of the producer's copies on the way out: the resident tiles and the
-// last two halves issued (one per stage).
+// last halves issued (one per stage).
+template <int STAGES>
 __device__ __forceinline__ void drain_loads(const View &v, int issued, uint64_t limit_ns) {
     mbar_wait_drain(v.once, 0, limit_ns);
-    for (int u = max(0, issued - kStages); u < issued; ++u)
-        mbar_wait_drain(&v.full[u & 1], (u >> 1) & 1, limit_ns);
+    for (int u = max(0, issued - STAGES); u < issued; ++u)
+        mbar_wait_drain(&v.full[u % STAGES], (u / STAGES) & 1, limit_ns);
+}
+
+// Copies the tile staged in R2 into TMEM [kTmOp, kTmOp + 128) and frees R2:
+// the copies complete at the first completion of the last stage's empty
+// barrier, which the issuing warp then waits for.
+template <int STAGES>
+__device__ __forceinline__ bool stage_to_tmem(const View &v, uint32_t tmem, const WaitCtl &ctl) {
+    tc_fence_after();
+    copy_tile_to_tmem(tmem + kTmOp, sdesc_sw128(smem_u32(v.c(kRegions - 1)), 16, 1024));
+    mma_commit_elect(&v.empty[STAGES - 1]);
+    return __all_sync(0xffffffffu, mbar_wait(&v.empty[STAGES - 1], 0, ctl, kSiteEmpty));
 }
 
 // acc (+)= A[tmem, 128 x 64 bf16] * B[64 rows x N, MN-major], the A pairs
@@ -228,22 +255,41 @@ __device__ __forceinline__ void load_rows(uint8_t *dst, int chunk_bytes, const C
 
 __device__ __forceinline__ void setup(const View &v) {
     mbar_init(v.once, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < 3; ++s) {
         mbar_init(&v.full[s], 1);
         mbar_init(&v.empty[s], 1);
     }
-    mbar_init(v.s_full, 1);
-    mbar_init(v.p_full, kEwWarps);
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(&v.s_full[b], 1);
+        mbar_init(&v.p_full[b], kEwWarps);
+    }
     mbar_init(v.o_full, 1);
     *v.abort_flag = 0;
     fence_mbarrier_init();
 }
 
 // ============================== dK / dV kernel ==============================
-template <bool CAUSAL>
+// Two CTAs per (K/V head, key block j): the dV CTA (even blockIdx) and the
+// dK CTA (odd).  Both hold K_j in TMEM [128, 256) and stream Q and dO in
+// 64-query halves; both compute S^T = K_j Q_h^T.
+//   * dV CTA: P^T = 2^(S^T c - LSE2) and dV += P^T dO_h (no dP, no dS).  S^T
+//     is double-buffered in TMEM ([0, 64) and [64, 128)), so S^T of the next
+//     half runs while the elementwise warps work on this one; three stages.
+//     TMEM: S^T x 2, K_j, dV [256, 512).
+//   * dK CTA: dP^T = V_j dO_h^T (V_j resident in R0), dS^T = P^T (dP^T - D),
+//     dK += dS^T Q_h.  TMEM: S^T [0, 64), dP^T [64, 128), K_j, dK [256, 512);
+//     one S^T / dP^T pair, so the elementwise step waits for the MMAs and
+//     the MMAs for it; two stages.
+template <bool DV>
+struct Role {
+    static constexpr int kStages = DV ? 3 : 2;
+};
+
+template <bool CAUSAL, bool DV>
 __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQh, const CUtensorMap *tmK,
                                             const CUtensorMap *tmV, const CUtensorMap *tmdOh,
                                             const Params &p, int bh, int jb, int lane) {
+    constexpr int S = Role<DV>::kStages;
     if (lane != 0) return;
     const View v = view();
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd256, p.limit_ns};
@@ -251,30 +297,31 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQh, const CUt
     const int n_q = p.n_blocks - i0;
     const int n_u = 2 * p.group * n_q;
     const uint64_t pol = l2_policy_evict_last();
-    mbar_arrive_expect_tx(v.once, 2 * kTile);
-    load_rows(v.a, kBox, tmV, v.once, jb * kBlk, bh, pol);         // V_j, resident
-    load_rows(v.c(1), kBox, tmK, v.once, jb * kBlk, bh, pol);      // K_j, for TMEM
+    mbar_arrive_expect_tx(v.once, DV ? kTile : 2 * kTile);
+    if (!DV) load_rows(v.c(0), kBox, tmV, v.once, jb * kBlk, bh, pol);  // V_j, resident
+    load_rows(v.c(kRegions - 1), kBox, tmK, v.once, jb * kBlk, bh, pol);  // K_j, for TMEM
     int issued = 0;
     for (int u = 0; u < n_u; ++u) {
-        if (!wait_stage_free(v, u, ctl)) break;
-        const int s = u & 1;
+        if (!wait_stage_free<S>(v, u, ctl)) break;
+        const int s = u % S, r = region_of<S>(u);
         const int t = u >> 1, g = t / n_q;
         const int qr = (i0 + t - g * n_q) * kBlk + (u & 1) * kHalf;  // the half's first query
         const int bq = q_head(p, bh, g);
         const size_t prow = static_cast<size_t>(bq) * p.n_blocks * kBlk + qr;
-        float *rows = v.rows + s * 2 * kHalf;
-        mbar_arrive_expect_tx(&v.full[s], 2 * kHTile + 2 * kHalf * 4);
-        load_rows(v.c(s), kHBox, tmQh, &v.full[s], qr, bq, pol);
-        load_rows(v.e(s), kHBox, tmdOh, &v.full[s], qr, bq, pol);
+        float *rows = v.rows(r);
+        mbar_arrive_expect_tx(&v.full[s], 2 * kHTile + (DV ? 1 : 2) * kHalf * 4);
+        load_rows(v.c(r), kHBox, tmQh, &v.full[s], qr, bq, pol);
+        load_rows(v.e(r), kHBox, tmdOh, &v.full[s], qr, bq, pol);
         bulk_load(rows, p.lse2 + prow, kHalf * 4, &v.full[s], pol);
-        bulk_load(rows + kHalf, p.dd + prow, kHalf * 4, &v.full[s], pol);
+        if (!DV) bulk_load(rows + kHalf, p.dd + prow, kHalf * 4, &v.full[s], pol);
         ++issued;
     }
-    drain_loads(v, issued, p.limit_ns);
+    drain_loads<S>(v, issued, p.limit_ns);
 }
 
-template <bool CAUSAL>
-__device__ __forceinline__ void dkdv_mma(const Params &p, int jb, int slice) {
+template <bool CAUSAL, bool DV>
+__device__ __forceinline__ void dkdv_mma(const Params &p, int jb) {
+    constexpr int S = Role<DV>::kStages;
     const View v = view();
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd256, p.limit_ns};
     const int n_u = 2 * p.group * (p.n_blocks - (CAUSAL ? jb : 0));
@@ -282,46 +329,62 @@ __device__ __forceinline__ void dkdv_mma(const Params &p, int jb, int slice) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t dV = sdesc_sw128(smem_u32(v.a), 16, 1024);
-    // K_j, staged in stage 1, into TMEM; its copies complete (and stage 1 is
-    // free) at the first completion of empty[1]
     bool ok = wait(v.once, 0, kSiteOnce);
-    if (ok) {
-        tc_fence_after();
-        copy_tile_to_tmem(tmem + kTmOp, sdesc_sw128(smem_u32(v.c(1)), 16, 1024));
-        mma_commit_elect(&v.empty[1]);
-        ok = wait(&v.empty[1], 0, kSiteEmpty);
-    }
-    for (int u = 0; u < n_u && ok; ++u) {
-        const int s = u & 1;
-        ok = wait(&v.full[s], (u >> 1) & 1, kSiteFull);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t dQh = sdesc_sw128(smem_u32(v.c(s)), 16, 1024);
-        const uint64_t ddOh = sdesc_sw128(smem_u32(v.e(s)), 16, 1024);
-        // the slice's two chunks of Q_h / dO_h as MN-major B operands (N =
-        // 128: chunks 2 slice and 2 slice + 1, kHBox apart)
-        const uint64_t dQs = sdesc_sw128(smem_u32(v.c(s) + 2 * slice * kHBox), kHBox, 1024);
-        const uint64_t ddOs = sdesc_sw128(smem_u32(v.e(s) + 2 * slice * kHBox), kHBox, 1024);
-        // S^T and dP^T of this half (the previous half's dV / dK, which read
-        // the same TMEM columns, were issued before by this thread)
-        mma_tmem_rows_k256(tmem + kTmS, tmem + kTmOp, dQh);
-        mma_rows_k256(tmem + kTmP, dV, ddOh);
-        mma_commit_elect(v.s_full);
-        ok = wait(v.p_full, u & 1, kSiteP);
-        if (!ok) break;
-        tc_fence_after();
-        mma_tmem_k64(tmem + kTmAcc, tmem + kTmS, ddOs, kIdescSlice, u > 0);             // dV_s
-        mma_tmem_k64(tmem + kTmAcc + 128, tmem + kTmS + 16, dQs, kIdescSlice, u > 0);  // dK_s
-        mma_commit_elect(&v.empty[s]);  // the stage is read
+    if (ok) ok = stage_to_tmem<S>(v, tmem, ctl);  // K_j
+    if (DV) {
+        // S^T(u + 1) into the other buffer before dV(u): the buffer last
+        // held P^T(u - 1), read by dV(u - 1), issued before by this thread
+        const auto issue_s = [&](int u) {
+            const bool good = wait(&v.full[u % S], (u / S) & 1, kSiteFull);
+            if (good) {
+                tc_fence_after();
+                mma_tmem_rows_k256(tmem + kTmS + 64 * (u & 1), tmem + kTmOp,
+                                   sdesc_sw128(smem_u32(v.c(region_of<S>(u))), 16, 1024));
+                mma_commit_elect(&v.s_full[u & 1]);
+            }
+            return good;
+        };
+        if (ok && n_u > 0) ok = issue_s(0);
+        for (int u = 0; u < n_u && ok; ++u) {
+            if (u + 1 < n_u) ok = issue_s(u + 1);
+            if (ok) ok = wait(&v.p_full[u & 1], (u >> 1) & 1, kSiteP);
+            if (!ok) break;
+            tc_fence_after();
+            // dV += P^T dO_h: dO_h as the MN-major B operand, N = 256
+            mma_tmem_k64(tmem + kTmAcc, tmem + kTmS + 64 * (u & 1),
+                         sdesc_sw128(smem_u32(v.e(region_of<S>(u))), kHBox, 1024), kIdescDq,
+                         u > 0);
+            mma_commit_elect(&v.empty[u % S]);  // the stage is read
+        }
+    } else {
+        const uint64_t dV = sdesc_sw128(smem_u32(v.c(0)), 16, 1024);
+        for (int u = 0; u < n_u && ok; ++u) {
+            const int s = u % S, r = region_of<S>(u);
+            ok = wait(&v.full[s], (u / S) & 1, kSiteFull);
+            if (!ok) break;
+            tc_fence_after();
+            // S^T and dP^T of this half (the previous half's dK, which read
+            // the same TMEM columns, was issued before by this thread)
+            mma_tmem_rows_k256(tmem + kTmS, tmem + kTmOp, sdesc_sw128(smem_u32(v.c(r)), 16, 1024));
+            mma_rows_k256(tmem + kTmP, dV, sdesc_sw128(smem_u32(v.e(r)), 16, 1024));
+            mma_commit_elect(&v.s_full[0]);
+            ok = wait(&v.p_full[0], u & 1, kSiteP);
+            if (!ok) break;
+            tc_fence_after();
+            // dK += dS^T Q_h: Q_h as the MN-major B operand, N = 256
+            mma_tmem_k64(tmem + kTmAcc, tmem + kTmS, sdesc_sw128(smem_u32(v.c(r)), kHBox, 1024),
+                         kIdescDq, u > 0);
+            mma_commit_elect(&v.empty[s]);  // the stage is read
+        }
     }
     mma_commit_elect(v.o_full);
     mbar_wait_drain(v.o_full, 0, p.limit_ns);
 }
 
-template <bool CAUSAL>
-__device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb, int slice,
-                                                 int warp, int lane) {
+template <bool CAUSAL, bool DV>
+__device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb, int warp,
+                                                 int lane) {
+    constexpr int S = Role<DV>::kStages;
     const View v = view();
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd256, p.limit_ns};
     const int N = p.N;
@@ -334,8 +397,8 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        const float *rows = v.rows + (u & 1) * 2 * kHalf + 32 * c;
-        ok = mbar_wait(&v.full[u & 1], (u >> 1) & 1, ctl, kSiteFull);  // the half's statistics
+        const float *rows = v.rows(region_of<S>(u)) + 32 * c;
+        ok = mbar_wait(&v.full[u % S], (u / S) & 1, ctl, kSiteFull);  // the half's statistics
         if (!ok) break;
         // this warp's 32 columns' statistics into registers before S^T is
         // ready (read during the math, they would wait on shared memory)
@@ -343,9 +406,10 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
 #pragma unroll
         for (int t4 = 0; t4 < 8; ++t4) {
             l4[t4] = *reinterpret_cast<const float4 *>(rows + 4 * t4);
-            d4[t4] = *reinterpret_cast<const float4 *>(rows + kHalf + 4 * t4);
+            if (!DV) d4[t4] = *reinterpret_cast<const float4 *>(rows + kHalf + 4 * t4);
         }
-        ok = mbar_wait(v.s_full, u & 1, ctl, kSiteS);
+        const int b = DV ? (u & 1) : 0;
+        ok = mbar_wait(&v.s_full[b], (DV ? (u >> 1) : u) & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
         const int t = u >> 1;
@@ -355,50 +419,68 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
         const int lim_lo = CAUSAL ? key - qh0 : 0;
         const int lim_hi = N - qh0;
         const bool masked = (CAUSAL && qi == 0) || qh0 + kHalf > N;
-        uint32_t sv[32], dv[32], pp[16], pds[16];
-        const uint32_t ts = tmem + lb + kTmS + 32 * c, tp = tmem + lb + kTmP + 32 * c;
-        tmem_ld32x2(ts, tp, sv, dv);
-        if (masked)
-            p_ds_masked(sv, dv, rows, rows + kHalf, true, 0.f, 0.f, p.scale_log2, lim_lo, lim_hi,
-                        32 * c, pp, pds);
-        else
-            p_ds_fast_reg(sv, dv, l4, d4, p.scale_log2, pp, pds);
-        tmem_st16(ts, pp);         // P^T over the first 16 of this warp's columns
-        tmem_st16(ts + 16, pds);   // dS^T over the next 16
+        const uint32_t ts = tmem + lb + kTmS + 64 * b + 32 * c;
+        uint32_t pp[16];
+        if (DV) {
+            uint32_t sv[32];
+            tmem_ld32(ts, sv);
+            p_only_reg(sv, l4, p.scale_log2, masked, lim_lo, lim_hi, 32 * c, pp);
+            tmem_st16(ts, pp);  // P^T over the first 16 of this warp's columns
+        } else {
+            uint32_t sv[32], dv[32], pds[16];
+            tmem_ld32x2(ts, tmem + lb + kTmP + 32 * c, sv, dv);
+            if (masked)
+                p_ds_masked(sv, dv, rows, rows + kHalf, true, 0.f, 0.f, p.scale_log2, lim_lo,
+                            lim_hi, 32 * c, pp, pds);
+            else
+                p_ds_fast_reg(sv, dv, l4, d4, p.scale_log2, pp, pds);
+            tmem_st16(ts, pds);  // dS^T over the first 16 of this warp's columns
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(v.p_full);
+        if (lane == 0) mbar_arrive(&v.p_full[b]);
     }
     if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
     if (ok) {
         tc_fence_after();
         // every lane takes part in the TMEM loads (warp-collective); only
-        // rows below N are stored
+        // rows below N are stored.  dV unscaled, dK times the scale.
         const bool in = key < N;
-        const size_t row = (static_cast<size_t>(bh) * N + key) * kD + 128 * slice;
-        __nv_bfloat16 *dvp = p.g1 + row, *dkp = p.g0 + row;
+        const float mul = DV ? 1.f : p.scale;
+        __nv_bfloat16 *dst = (DV ? p.g1 : p.g0) + (static_cast<size_t>(bh) * N + key) * kD;
 #pragma unroll 1
-        for (int g = 2 * c; g < 2 * c + 2; ++g) {  // 64 of the slice's 128 columns
-            uint32_t a[32], b[32], pa[16], pb[16];
+        for (int g = 4 * c; g < 4 * c + 4; ++g) {  // half of the 256 columns
+            uint32_t a[32], pa[16];
             tmem_ld32(tmem + lb + kTmAcc + 32 * g, a);
-            tmem_ld32(tmem + lb + kTmAcc + 128 + 32 * g, b);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                pa[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-                pb[e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale,
-                                    __uint_as_float(b[2 * e + 1]) * p.scale);
-            }
+            for (int e = 0; e < 16; ++e)
+                pa[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
+                                    __uint_as_float(a[2 * e + 1]) * mul);
             if (in) {
-                uint4 *o0 = reinterpret_cast<uint4 *>(dvp + 32 * g);
-                uint4 *o1 = reinterpret_cast<uint4 *>(dkp + 32 * g);
+                uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * g);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o0[e] = make_uint4(pa[4 * e], pa[4 * e + 1], pa[4 * e + 2], pa[4 * e + 3]);
-                    o1[e] = make_uint4(pb[4 * e], pb[4 * e + 1], pb[4 * e + 2], pb[4 * e + 3]);
-                }
+                for (int e = 0; e < 4; ++e)
+                    o[e] = make_uint4(pa[4 * e], pa[4 * e + 1], pa[4 * e + 2], pa[4 * e + 3]);
             }
         }
+    }
+}
+
+template <bool CAUSAL, bool DV>
+__device__ __forceinline__ void dkdv_role(const CUtensorMap *tmQh, const CUtensorMap *tmK,
+                                          const CUtensorMap *tmV, const CUtensorMap *tmdOh,
+                                          const Params &p, int bh, int jb, int warp, int lane) {
+    if (warp >= kMmaWarp) {
+        regs_decrease<kRegsCtl>();
+        if (warp == kTmaWarp)
+            dkdv_producer<CAUSAL, DV>(tmQh, tmK, tmV, tmdOh, p, bh, jb, lane);
+        else if (warp == kMmaWarp)
+            dkdv_mma<CAUSAL, DV>(p, jb);
+        __syncwarp();
+    } else {
+        regs_increase<kRegsEw>();
+        dkdv_elementwise<CAUSAL, DV>(p, bh, jb, warp, lane);
     }
 }
 
@@ -410,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmdOh, const Params p) {
     const View v = view();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slice = static_cast<int>(blockIdx.x & 1);  // the pair of a key block's slices
+    const bool dv_cta = (blockIdx.x & 1) == 0;  // the pair of a key block: dV, then dK
     int bh, jb;
     block_of<CAUSAL, true>(p, static_cast<int>(blockIdx.x >> 1), bh, jb);
     if (threadIdx.x == 0) setup(v);
@@ -421,17 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp >= kMmaWarp) {
-        regs_decrease<kRegsCtl>();
-        if (warp == kTmaWarp)
-            dkdv_producer<CAUSAL>(&tmQh, &tmK, &tmV, &tmdOh, p, bh, jb, lane);
-        else if (warp == kMmaWarp)
-            dkdv_mma<CAUSAL>(p, jb, slice);
-        __syncwarp();
-    } else {
-        regs_increase<kRegsEw>();
-        dkdv_elementwise<CAUSAL>(p, bh, jb, slice, warp, lane);
-    }
+    if (dv_cta)
+        dkdv_role<CAUSAL, true>(&tmQh, &tmK, &tmV, &tmdOh, p, bh, jb, warp, lane);
+    else
+        dkdv_role<CAUSAL, false>(&tmQh, &tmK, &tmV, &tmdOh, p, bh, jb, warp, lane);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -452,18 +527,18 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     const int bk = kv_head(p, bh);
     const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(v.once, 2 * kTile);
-    load_rows(v.a, kBox, tmdO, v.once, ib * kBlk, bh, pol_q);    // dO_i, resident
-    load_rows(v.c(1), kBox, tmQ, v.once, ib * kBlk, bh, pol_q);  // Q_i, for TMEM
+    load_rows(v.c(0), kBox, tmdO, v.once, ib * kBlk, bh, pol_q);             // dO_i, resident
+    load_rows(v.c(kRegions - 1), kBox, tmQ, v.once, ib * kBlk, bh, pol_q);  // Q_i, for TMEM
     int issued = 0;
     for (int u = 0; u < n_u; ++u) {
-        if (!wait_stage_free(v, u, ctl)) break;
-        const int s = u & 1;
+        if (!wait_stage_free<2>(v, u, ctl)) break;
+        const int s = u & 1, r = region_of<2>(u);
         mbar_arrive_expect_tx(&v.full[s], 2 * kHTile);
-        load_rows(v.c(s), kHBox, tmKh, &v.full[s], u * kHalf, bk, pol_kv);
-        load_rows(v.e(s), kHBox, tmVh, &v.full[s], u * kHalf, bk, pol_kv);
+        load_rows(v.c(r), kHBox, tmKh, &v.full[s], u * kHalf, bk, pol_kv);
+        load_rows(v.e(r), kHBox, tmVh, &v.full[s], u * kHalf, bk, pol_kv);
         ++issued;
     }
-    drain_loads(v, issued, p.limit_ns);
+    drain_loads<2>(v, issued, p.limit_ns);
 }
 
 template <bool CAUSAL>
@@ -475,27 +550,21 @@ __device__ __forceinline__ void dq_mma(const Params &p, int ib) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    const uint64_t ddO = sdesc_sw128(smem_u32(v.a), 16, 1024);
-    // Q_i, staged in stage 1, into TMEM (as in the dK / dV kernel)
+    const uint64_t ddO = sdesc_sw128(smem_u32(v.c(0)), 16, 1024);
     bool ok = wait(v.once, 0, kSiteOnce);
-    if (ok) {
-        tc_fence_after();
-        copy_tile_to_tmem(tmem + kTmOp, sdesc_sw128(smem_u32(v.c(1)), 16, 1024));
-        mma_commit_elect(&v.empty[1]);
-        ok = wait(&v.empty[1], 0, kSiteEmpty);
-    }
+    if (ok) ok = stage_to_tmem<2>(v, tmem, ctl);  // Q_i
     for (int u = 0; u < n_u && ok; ++u) {
-        const int s = u & 1;
+        const int s = u & 1, r = region_of<2>(u);
         ok = wait(&v.full[s], (u >> 1) & 1, kSiteFull);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t dKh = sdesc_sw128(smem_u32(v.c(s)), 16, 1024);
-        const uint64_t dVh = sdesc_sw128(smem_u32(v.e(s)), 16, 1024);
-        const uint64_t dKmn = sdesc_sw128(smem_u32(v.c(s)), kHBox, 1024);  // MN-major B, N = 256
+        const uint64_t dKh = sdesc_sw128(smem_u32(v.c(r)), 16, 1024);
+        const uint64_t dVh = sdesc_sw128(smem_u32(v.e(r)), 16, 1024);
+        const uint64_t dKmn = sdesc_sw128(smem_u32(v.c(r)), kHBox, 1024);  // MN-major B, N = 256
         mma_tmem_rows_k256(tmem + kTmS, tmem + kTmOp, dKh);  // S = Q K_h^T
         mma_rows_k256(tmem + kTmP, ddO, dVh);                // dP = dO V_h^T
-        mma_commit_elect(v.s_full);
-        ok = wait(v.p_full, u & 1, kSiteP);
+        mma_commit_elect(&v.s_full[0]);
+        ok = wait(&v.p_full[0], u & 1, kSiteP);
         if (!ok) break;
         tc_fence_after();
         mma_tmem_k64(tmem + kTmAcc, tmem + kTmS, dKmn, kIdescDq, u > 0);  // dQ += dS K_h
@@ -520,7 +589,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
     const float my_nl2 = p.lse2[prow], my_nd = p.dd[prow];
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        ok = mbar_wait(v.s_full, u & 1, ctl, kSiteS);
+        ok = mbar_wait(&v.s_full[0], u & 1, ctl, kSiteS);
         if (!ok) break;
         tc_fence_after();
         const int k0 = u * kHalf;  // the half's first key
@@ -539,7 +608,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(v.p_full);
+        if (lane == 0) mbar_arrive(&v.p_full[0]);
     }
     if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
     if (ok) {
@@ -634,7 +703,7 @@ static int launch_bwd256_t(const BwdArgs &a, const float *lse2, const float *dd,
         return static_cast<long long>(n_blocks) * heads;
     };
     const long long bh_kv = a.BH / p.group;
-    // dK / dV: two CTAs (d-slices) per (K/V head, key block)
+    // dK / dV: two CTAs (dV's, then dK's) per (K/V head, key block)
     const long long grid1 = 2 * set_heads(bh_kv);
     if (grid1 > 0x7FFFFFFFLL) return FA_ERR_SHAPE;
     p.g0 = static_cast<__nv_bfloat16 *>(a.dK);
