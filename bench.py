@@ -179,18 +179,43 @@ def row_flops(rows: np.ndarray, N: int, d: int, causal: bool) -> float:
     return float(4.0 * d * N * rows.size)
 
 
-def oracle_sample(w, causal, q, k, v, rows_per_head, nthreads, offset=0):
+def oracle_sample(w, causal, q, k, v, rows_per_head, nthreads, offset=0, keep=None):
     """Time the fp64 oracle on `rows_per_head` evenly spread rows of every
-    head; returns (seconds, nominal FLOPs of those rows)."""
+    head; returns (seconds, nominal FLOPs of those rows).  With a dict as
+    `keep`, also leaves the rows and the oracle's O and LSE there."""
     import oracle
     BH = w.B * w.H
     stride = max(1, w.N // rows_per_head)
     base = (np.arange(rows_per_head, dtype=np.int64) * stride + offset) % w.N
     rows = np.broadcast_to(base, (BH, rows_per_head)).copy()
     t0 = time.perf_counter()
-    oracle.attention_fwd(q, k, v, causal=causal, scale=w.scale, rows=rows, nthreads=nthreads)
+    o_ref, l_ref = oracle.attention_fwd(q, k, v, causal=causal, scale=w.scale, rows=rows,
+                                        nthreads=nthreads)
     dt = time.perf_counter() - t0
+    if keep is not None:
+        keep.update(rows=rows, o=o_ref, lse=l_ref)
     return dt, row_flops(rows, w.N, w.d, causal)
+
+
+# The output contract: O max-abs and mean-abs error, LSE abs error against
+# the fp64 oracle (bf16 output, fp32 accumulation).
+PARITY_BOUNDS = {"o_max_abs": 2e-2, "o_mean_abs": 2e-3, "lse_max_abs": 1e-3}
+
+
+def sample_parity(o_gpu, lse_gpu, rows, o_ref, l_ref):
+    """Error of the GPU output (O bf16 [B,H,N,d], LSE fp32 [B,H,N], device or
+    host tensors) on the oracle's sampled rows [B*H, R]."""
+    BH, R = rows.shape
+    o = o_gpu.float().cpu().numpy().reshape(BH, -1, o_gpu.shape[-1])
+    lse = lse_gpu.float().cpu().numpy().reshape(BH, -1)
+    o_s = np.take_along_axis(o, rows[:, :, None], axis=1)
+    l_s = np.take_along_axis(lse, rows, axis=1)
+    eo = np.abs(o_s - o_ref.reshape(BH, R, -1))
+    el = np.abs(l_s - l_ref.reshape(BH, R))
+    got = {"o_max_abs": float(eo.max()), "o_mean_abs": float(eo.mean()),
+           "lse_max_abs": float(el.max())}
+    return {"rows": int(BH * R), **got, "bounds": PARITY_BOUNDS,
+            "within_bounds": all(got[key] <= PARITY_BOUNDS[key] for key in got)}
 
 
 def oracle_inputs(w):
@@ -225,19 +250,25 @@ def host_cpu() -> str:
     return f"{platform.machine()} {name} x{os.cpu_count()}".strip()
 
 
-def cpu_baseline(w, causal, target_s=15.0):
+def cpu_baseline(w, causal, target_s=15.0, gpu_out=None):
+    """The oracle timed on a bounded sample of the workload's rows; with the
+    GPU's (O, LSE) of the same inputs, also their error on those rows."""
     import oracle
     qf, kf, vf = oracle_inputs(w)
     nth = oracle.default_threads()
     dt, _ = oracle_sample(w, causal, qf, kf, vf, 8, nth)  # calibration
     per_row = dt / 8
     rph = int(min(w.N, max(8, target_s / max(per_row, 1e-6))))
-    dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
-            "cpu": host_cpu(),
-            "sample": f"{rph} evenly spaced query rows in each of the {w.B * w.H} heads "
-                      f"({rph * w.B * w.H} rows, {dt:.1f} s); fp64, S and P materialised "
-                      f"over all N keys per row; FLOPs counted as 4*d per attended key"}
+    ref = {}
+    dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth, keep=ref)
+    out = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
+           "cpu": host_cpu(),
+           "sample": f"{rph} evenly spaced query rows in each of the {w.B * w.H} heads "
+                     f"({rph * w.B * w.H} rows, {dt:.1f} s); fp64, S and P materialised "
+                     f"over all N keys per row; FLOPs counted as 4*d per attended key"}
+    if gpu_out is not None:
+        out["parity"] = sample_parity(*gpu_out, ref["rows"], ref["o"], ref["lse"])
+    return out
 
 
 def run_reference(args, w, causal):
@@ -398,7 +429,8 @@ def run_ours(args, w, causal):
     if ws == 1 and not args.no_secondary:
         out["secondary"] = secondary_legs(dev, fa, peak, peak_kind)
     if ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, causal)
+        # the timed launches' output (every set holds the same inputs)
+        out["cpu_baseline"] = cpu_baseline(w, causal, gpu_out=(sets[0][3], sets[0][4]))
     print(json.dumps(out), flush=True)
 
 
@@ -437,7 +469,7 @@ def secondary_legs(dev, fa, peak, peak_kind):
     out = {}
     status = []
 
-    def fwd_leg(name, steps, e2e_steps=0):
+    def fwd_leg(name, steps, e2e_steps=0, keep=None):
         w = WORKLOADS[name]
         causal = w.causal[-1]
         q, k, v = make_workload(w)
@@ -458,6 +490,8 @@ def secondary_legs(dev, fa, peak, peak_kind):
                "kernel_ms_median": statistics.median(per),
                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
                             "frac": tf / peak, "peak_source": f"bf16_tflops of {peak_kind}"}}
+        if keep is not None:
+            keep["gpu"] = (outs[0][0].cpu(), outs[0][1].cpu())
         del sets, outs
         if e2e_steps:
             host = fa.fa_fwd_host_gqa if gqa else fa.fa_fwd_host
@@ -486,23 +520,28 @@ def secondary_legs(dev, fa, peak, peak_kind):
     for name, rph in (("batch", 16), ("long", 0)):
         w = WORKLOADS[name]
         causal = w.causal[-1]
-        leg = fwd_leg(name, 50 if name == "batch" else 20)
+        kept = {}
+        leg = fwd_leg(name, 50 if name == "batch" else 20, keep=kept)
         qf, kf, vf = oracle_inputs(w)
         nth = oracle.default_threads()
+        ref = {}
         if rph:
-            dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth)
+            dt, fl = oracle_sample(w, causal, qf, kf, vf, rph, nth, keep=ref)
             what = f"{rph} evenly spaced rows in each of the {w.B * w.H} heads"
         else:
             from online_softmax_fa_gb300.inputs import sample_rows
             rows = sample_rows(w.N, w.B * w.H, w.sampled_rows, seed=w.seed)
             t0 = time.perf_counter()
-            oracle.attention_fwd(qf, kf, vf, causal=causal, scale=w.scale, rows=rows,
-                                 nthreads=nth)
+            o_ref, l_ref = oracle.attention_fwd(qf, kf, vf, causal=causal, scale=w.scale,
+                                                rows=rows, nthreads=nth)
             dt = time.perf_counter() - t0
+            ref.update(rows=rows, o=o_ref, lse=l_ref)
             fl = row_flops(rows, w.N, w.d, causal)
             what = f"the parity sample: {rows.shape[1]} rows in each of the {w.B * w.H} heads"
         leg["oracle"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "seconds": dt,
-                         "cores": nth, "sample": what}
+                         "cores": nth, "sample": what,
+                         "parity": sample_parity(*kept["gpu"], ref["rows"], ref["o"],
+                                                 ref["lse"])}
         out[f"{name}_forward"] = leg
         del qf, kf, vf
 
