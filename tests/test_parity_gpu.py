@@ -241,7 +241,10 @@ def _sampled_check(fa, w, rows_per_head, causal):
     O_ref, L_ref = oracle.attention_fwd(q.reshape(BH, w.N, w.d), k.reshape(BH, w.N, w.d),
                                         v.reshape(BH, w.N, w.d), causal=causal,
                                         scale=w.scale, rows=rows)
-    return check(o[idx, rows], lse[idx, rows], O_ref, L_ref, w.name)
+    mx, mean, lmx = check(o[idx, rows], lse[idx, rows], O_ref, L_ref, w.name)
+    print(f"{w.name} sampled ({rows.size} rows): O max {mx:.4e} mean {mean:.4e} "
+          f"LSE max {lmx:.4e}")
+    return mx, mean, lmx
 
 
 def _full_check(fa, w, causal):
