@@ -32,9 +32,9 @@
 //     and V, 64 KB) through two stages.  Per half: S and dP (N = 64), dS
 //     (thread = query row), then dQ += dS K_h as one M128 x N256 MMA per 16
 //     keys.  TMEM: S [0, 64), dP [64, 128), Q_i [128, 256), dQ [256, 512).
-// TMEM holds one S^T / dP^T pair, so a half's MMAs wait for the elementwise
-// step of the previous half.  The kernels are deterministic (no atomics,
-// fixed order).  Causal: blocks above the diagonal are skipped, the
+// In the dK CTA and in dQ, TMEM holds one S^T / dP^T (S / dP) pair, so a
+// half's MMAs wait for the elementwise step of the previous half.  The
+// kernels are deterministic (no atomics, fixed order).  Causal: blocks above the diagonal are skipped, the
 // diagonal block and a ragged last block masked per element.
 #include <cuda.h>
 #include <cuda_bf16.h>
