@@ -395,10 +395,15 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
     const int quarter = warp & 3, c = warp >> 2;  // c: queries [32c, 32c + 32) of each half
     const int key = jb * kBlk + quarter * 32 + lane;
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
+    // wait results made warp-uniform: the warp reaches its collective TMEM
+    // loads together or not at all
+    const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
+    };
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
         const float *rows = v.rows(region_of<S>(u)) + 32 * c;
-        ok = mbar_wait(&v.full[u % S], (u / S) & 1, ctl, kSiteFull);  // the half's statistics
+        ok = wait(&v.full[u % S], (u / S) & 1, kSiteFull);  // the half's statistics
         if (!ok) break;
         // this warp's 32 columns' statistics into registers before S^T is
         // ready (read during the math, they would wait on shared memory)
@@ -409,7 +414,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
             if (!DV) d4[t4] = *reinterpret_cast<const float4 *>(rows + kHalf + 4 * t4);
         }
         const int b = DV ? (u & 1) : 0;
-        ok = mbar_wait(&v.s_full[b], (DV ? (u >> 1) : u) & 1, ctl, kSiteS);
+        ok = wait(&v.s_full[b], (DV ? (u >> 1) : u) & 1, kSiteS);
         if (!ok) break;
         tc_fence_after();
         const int t = u >> 1;
@@ -441,7 +446,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
         __syncwarp();
         if (lane == 0) mbar_arrive(&v.p_full[b]);
     }
-    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) ok = wait(v.o_full, 0, kSiteO);
     if (ok) {
         tc_fence_after();
         // every lane takes part in the TMEM loads (warp-collective); only
@@ -589,7 +594,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
     const float my_nl2 = p.lse2[prow], my_nd = p.dd[prow];
     bool ok = true;
     for (int u = 0; u < n_u && ok; ++u) {
-        ok = mbar_wait(&v.s_full[0], u & 1, ctl, kSiteS);
+        ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[0], u & 1, ctl, kSiteS));
         if (!ok) break;
         tc_fence_after();
         const int k0 = u * kHalf;  // the half's first key
@@ -610,7 +615,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
         __syncwarp();
         if (lane == 0) mbar_arrive(&v.p_full[0]);
     }
-    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(v.o_full, 0, ctl, kSiteO));
     if (ok) {
         tc_fence_after();
         // every lane takes part in the TMEM loads (warp-collective); only

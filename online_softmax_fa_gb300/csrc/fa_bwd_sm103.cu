@@ -439,7 +439,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
         // the stage's LSE2/D rows landed with its tiles (the stage cannot
         // be refilled before this block's last dV / dK); this warp's 32
         // columns of them go to registers before S^T / dP^T are waited for
-        ok = mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ);
+        ok = __all_sync(0xffffffffu, mbar_wait(&v.full[s], (t / C::kStages) & 1, ctl, kSiteQ));
         if (!ok) break;
         const int qi = t % n_q;  // query block within the current query head
         const int q0 = (i0 + qi) * kBlk;
@@ -451,7 +451,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
             l4[e] = reinterpret_cast<const float4 *>(lse2)[e];
             d4[e] = reinterpret_cast<const float4 *>(dd)[e];
         }
-        ok = mbar_wait(&v.s_full[h], (u >> 1) & 1, ctl, kSiteS);
+        ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[h], (u >> 1) & 1, ctl, kSiteS));
         if (!ok) break;
         tc_fence_after();
         // column (query) q kept iff q < N and, causal, q >= key
@@ -477,7 +477,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
         __syncwarp();
         if (lane == 0) mbar_arrive(&v.p_full[h]);
     }
-    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(v.o_full, 0, ctl, kSiteO));
     if (ok) {
         tc_fence_after();
         const bool in = key < N;
@@ -685,7 +685,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
     const float my_nd = p.dd[prow];     // -D
     bool ok = true;
     for (int t = 0; t < n_k && ok; ++t) {
-        ok = mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS);
+        ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS));
         if (!ok) break;
         tc_fence_after();
         const int k0 = t * kBlk;
@@ -717,7 +717,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
         __syncwarp();
         if (lane == 0) mbar_arrive(v.p_full);
     }
-    if (ok) ok = mbar_wait(v.o_full, 0, ctl, kSiteO);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(v.o_full, 0, ctl, kSiteO));
     if (ok) {
         tc_fence_after();
         __nv_bfloat16 *dq = p.g0 + (static_cast<size_t>(bh) * N + q) * D;
