@@ -431,7 +431,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         // kStaleMax, so p <= 2^kStaleMax
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < w.n; ++j, ++t) {
-            ok = mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS);
+            ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS));
             if (!ok) break;
             tc_fence_after();
             const uint32_t tm_s = tmem + lane_bits + kTmS + (t & 1) * kBlockN;
@@ -510,7 +510,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         }
         if (!ok) break;
         // ---- epilogue: O = a / l (bf16), LSE = (m + log2 l) ln 2
-        ok = mbar_wait(v.o_full, r & 1, ctl, kSiteOFull);
+        ok = __all_sync(0xffffffffu, mbar_wait(v.o_full, r & 1, ctl, kSiteOFull));
         if (!ok) break;
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

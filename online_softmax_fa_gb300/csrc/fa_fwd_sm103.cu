@@ -596,7 +596,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         float m = -INFINITY;
         float l = 0.f;
         for (int j = 0; j < n_k; ++j) {
-            ok = mbar_wait(s_full, sc & 1, ctl, kSiteSFull);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full, sc & 1, ctl, kSiteSFull));
             if (!ok) break;
             ++sc;
             tc_fence_after();
@@ -672,7 +672,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         if (!ok) break;
 
         // ---- epilogue: O = a / l (bf16), LSE = (m + log2 l) ln 2
-        ok = mbar_wait(o_full, r & 1, ctl, kSiteOFull);
+        ok = __all_sync(0xffffffffu, mbar_wait(o_full, r & 1, ctl, kSiteOFull));
         if (!ok) break;
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
