@@ -1,10 +1,10 @@
 /*
  * fa_debug.h -- extra entry points of the debug build of the library
- * (_build/libfa_gb300_debug.so, the forward kernel compiled with FA_DEBUG).
+ * (_build/libfa_gb300_debug.so, the forward kernels compiled with FA_DEBUG).
  *
  * The debug build exports everything fa.h declares and behaves like the
- * release build, with one difference: the forward kernel for head
- * dimensions 64 and 128 checks each index it computes before using it:
+ * release build, with one difference: the forward kernels (head dimensions
+ * 64, 128 and 256) check each index they compute before using it:
  *   - the work item id, from the grid or a cancelled CTA;
  *   - the head and row coordinates of every Q, K and V tensor-map load;
  *   - the shared-memory ranges that the loads write and the MMAs read;
@@ -15,10 +15,11 @@
  * word; the first error wins.  The access is skipped, and the CTA's abort
  * flag is raised so the CTA's other warps stop at their next wait.  No
  * check traps.  fa_device_error then returns FA_ERR_CHECK, and
- * fa_last_device_status returns (1 << 8) | 0x80 | n, where n is:
+ * fa_last_device_status returns (k << 8) | 0x80 | n, with k = 1 for the
+ * d 64/128 kernel and 2 for the d = 256 one, and n:
  *   1 item id, 2 Q load, 3 K/V load, 4 shared memory, 5 tensor memory,
  *   6 O store, 7 LSE store.
- * Every other kernel (d = 256, backward, decoding) is the release code.
+ * The other kernels (backward, decoding) are the release code.
  * The checks follow the kernel's own design: one CTA per
  * (batch, head, query block) work item, tiled over key blocks
  * ("Understanding FlashAttention Pt 1" (wpnews.pro), section 2.4, and
@@ -38,8 +39,9 @@ extern "C" {
 typedef enum {
     FA_DEBUG_NONE = 0,           /* disarm */
     /* The producer of work item `a` (a CTA's first item is its grid index)
-     * skips the load of key tile `b` (0-based) and the arrival on that
-     * tile's barrier, as if the arrival had been lost.  The waits that
+     * skips the load of key tile `b` (0-based; at d = 256 the tile's first
+     * half of K columns) and the arrival on that tile's barrier, as if the
+     * arrival had been lost.  The waits that
      * depend on the tile run out after the launch's limit: the kernel
      * drains its copies, frees its tensor memory and exits, and
      * fa_device_error returns FA_ERR_TIMEOUT. */
@@ -52,9 +54,9 @@ typedef enum {
 } fa_debug_fault;
 
 /*
- * fa_debug_arm -- arms one fault for the next launch of the forward kernel
- * for head dimension 64 or 128 made by this process (fa_fwd, fa_fwd_gqa,
- * or the host-buffer variants).  That launch disarms it.  While a fault is
+ * fa_debug_arm -- arms one fault for the next launch of a forward kernel
+ * (any head dimension) made by this process (fa_fwd, fa_fwd_gqa, or the
+ * host-buffer variants).  That launch disarms it.  While a fault is
  * armed, `limit_us` (1 .. 1000000) replaces that launch's time limit per
  * wait (2 s); 0 keeps the default.  Host-only: it enqueues nothing and
  * needs no GPU.

@@ -37,6 +37,10 @@
 
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
+#include "debug_checks.cuh"
+#ifdef FA_DEBUG
+#include "../../include/fa_debug.h"
+#endif
 
 namespace fa {
 
@@ -93,6 +97,12 @@ struct Params {
     int first_group;  // heads in the first (partial) group
     float scale_log2;
     uint64_t limit_ns;
+    // debug build only: the extent (rows of O and LSE) the store checks
+    // use, and an injected fault -- the producer of item lose_item skips the
+    // load of the first K half of key tile lose_tile and the arrival on its
+    // barrier (-1: none)
+    long long o_rows;
+    int lose_item, lose_tile;
 };
 
 struct View {
@@ -140,6 +150,11 @@ struct Work {
     int bh, kvh, qb, n;  // n: key tiles this query block needs
 };
 
+// Debug checks: a range inside this kernel's shared memory.
+__device__ __forceinline__ bool in_smem_256(const void *ptr, int bytes) {
+    return in_smem(ptr, bytes, kSmemBytes);
+}
+
 // Work item x (the grid's CTA index, in priority order) -> (head, query
 // block), as in the d <= 128 kernel: causal, heads in groups (the partial
 // group first) and inside a group the heaviest query block first with the
@@ -180,12 +195,13 @@ __device__ __forceinline__ Work work_of(const Params &p, int x) {
 // more work).  Called by every thread of a consumer warp; one lane then
 // frees the slot.
 __device__ __forceinline__ bool next_item(const View &v, const WaitCtl &ctl, int r, int lane,
-                                          int &x) {
+                                          int n_items, int &x) {
     const int slot = r & 1;
     if (!__all_sync(0xffffffffu, mbar_wait(&v.sched_full[slot], (r >> 1) & 1, ctl,
                                            kSiteSchedFull)))
         return false;
     x = v.sched_item[slot];
+    if (x >= 0 && !dbg_ok(x < n_items, ctl, kChkItem)) x = -1;
     __syncwarp();
     if (lane == 0) mbar_arrive(&v.sched_empty[slot]);
     return true;
@@ -213,6 +229,7 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
             ok = mbar_wait(&v.sched_empty[slot], ((r >> 1) & 1) ^ 1, ctl, kSiteSchedEmpty);
             if (!ok) break;
         }
+        if (x >= 0 && !dbg_ok(x < p.n_items, ctl, kChkItem)) x = -1;  // end the work
         v.sched_item[slot] = x;
         mbar_arrive(&v.sched_full[slot]);
         if (x < 0) break;
@@ -220,6 +237,12 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
         if (r > 0) {  // the previous item's last S has read Q
             ok = mbar_wait(v.q_empty, (r - 1) & 1, ctl, kSiteQEmpty);
             if (!ok) break;
+        }
+        if (!dbg_ok(w.bh >= 0 && w.bh < p.BH && w.qb >= 0 && w.qb < p.n_qblocks, ctl,
+                    kChkTmaQ) ||
+            !dbg_ok(in_smem_256(v.q, kQBytes), ctl, kChkSmem)) {
+            ok = false;
+            break;
         }
         mbar_arrive_expect_tx(v.q_full, kQBytes);
         {
@@ -241,10 +264,20 @@ __device__ __forceinline__ void role_load_qk(const CUtensorMap *tmQ, const CUten
                 if (u >= kStagesK)
                     ok = mbar_wait(&v.k_empty[s], ((u / kStagesK) & 1) ^ 1, ctl, kSiteKEmpty);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&v.k_full[s], kKStage);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_3d(v.k + s * kKStage + c * kBox, tmK, &v.k_full[s],
-                                64 * (2 * h + c), j * kBlockN, w.kvh, pol_kv);
+                if (!dbg_ok(j * kBlockN < p.N && w.kvh >= 0 && w.kvh < p.BH / p.group, ctl,
+                            kChkTmaKV) ||
+                    !dbg_ok(in_smem_256(v.k + s * kKStage, kKStage), ctl, kChkSmem)) {
+                    ok = false;
+                    break;
+                }
+                // debug build: an injected fault loses this K half's load and
+                // its arrival (the consumers' waits then run out)
+                if (!(kDebug && x == p.lose_item && j == p.lose_tile && h == 0)) {
+                    mbar_arrive_expect_tx(&v.k_full[s], kKStage);
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d(v.k + s * kKStage + c * kBox, tmK, &v.k_full[s],
+                                    64 * (2 * h + c), j * kBlockN, w.kvh, pol_kv);
+                }
                 ++u;
             }
         }
@@ -276,7 +309,7 @@ __device__ __forceinline__ void role_load_v(const CUtensorMap *tmV64, const Para
     bool ok = true;
     for (int r = 0; ok; ++r) {
         int x;
-        ok = next_item(v, ctl, r, lane, x);
+        ok = next_item(v, ctl, r, lane, p.n_items, x);
         if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         if (lane == 0) {
@@ -288,6 +321,12 @@ __device__ __forceinline__ void role_load_v(const CUtensorMap *tmV64, const Para
                         ok = mbar_wait(&v.v_empty[s], ((u / kStagesV) & 1) ^ 1, ctl,
                                        kSiteVEmpty);
                     if (!ok) break;
+                    if (!dbg_ok(j < p.n_ktiles && w.kvh >= 0 && w.kvh < p.BH / p.group, ctl,
+                                kChkTmaKV) ||
+                        !dbg_ok(in_smem_256(v.v + s * kVStage, kVStage), ctl, kChkSmem)) {
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(&v.v_full[s], kVStage);
                     for (int c = 0; c < 4; ++c)
                         tma_load_3d(v.v + s * kVStage + c * kVBox, tmV64, &v.v_full[s],
@@ -319,6 +358,11 @@ __device__ __forceinline__ void role_mma(const Params &p) {
     };
     int uk = 0, uv = 0;  // K / V halves consumed, across items
     int t = 0;           // key tiles processed, across items (S buffer t & 1)
+    const bool layout_ok =
+        dbg_ok(whole_tmem(tmem), ctl, kChkTmem) &&
+        dbg_ok(in_smem_256(v.q, kQBytes) && in_smem_256(v.k, kStagesK * kKStage) &&
+                   in_smem_256(v.v, kStagesV * kVStage),
+               ctl, kChkSmem);
     // S(t) = Q K^T: 16 K-steps over d, two K halves of 8 steps each.
     const auto issue_s = [&](int tt) -> bool {
         const uint32_t d_tm = tmem + kTmS + (tt & 1) * kBlockN;
@@ -340,10 +384,10 @@ __device__ __forceinline__ void role_mma(const Params &p) {
         return true;
     };
     const int lane = static_cast<int>(threadIdx.x & 31);
-    bool ok = true;
+    bool ok = layout_ok;
     for (int r = 0; ok; ++r) {
         int x;
-        ok = next_item(v, ctl, r, lane, x);
+        ok = next_item(v, ctl, r, lane, p.n_items, x);
         if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         ok = wait(v.q_full, r & 1, kSiteQ);
@@ -419,10 +463,10 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
     const float cs = p.scale_log2;
     const uint64_t cs2 = f2_pack(cs, cs);
     int t = 0;  // key tiles consumed, across items
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int r = 0; ok; ++r) {
         int x;
-        ok = next_item(v, ctl, r, lane, x);
+        ok = next_item(v, ctl, r, lane, p.n_items, x);
         if (!ok || x < 0) break;
         const Work w = work_of<CAUSAL>(p, x);
         const int qrow = w.qb * kBlockM + row;
@@ -515,6 +559,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const bool in_range = qrow < N;
+        const long long row_flat = static_cast<long long>(w.bh) * N + qrow;
         __nv_bfloat16 *orow = p.O + (static_cast<size_t>(w.bh) * N + qrow) * kD;
 #pragma unroll 1
         for (int c = 0; c < kD / 32; ++c) {
@@ -525,7 +570,10 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
             for (int e = 0; e < 16; ++e)
                 pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
                                     __uint_as_float(o[2 * e + 1]) * inv_l);
-            if (in_range) {
+            if (in_range &&
+                dbg_ok(row_flat < p.o_rows &&
+                           (reinterpret_cast<uintptr_t>(orow + 32 * c) & 15u) == 0,
+                       ctl, kChkStoreO)) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -535,7 +583,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(v.o_empty);  // O may be overwritten by the next item
-        if (in_range) {
+        if (in_range && dbg_ok(row_flat < p.o_rows, ctl, kChkStoreLse)) {
             const float lse = (l > 0.f) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
             p.LSE[static_cast<size_t>(w.bh) * N + qrow] = lse;
         }
@@ -633,6 +681,21 @@ static int launch_256_t(const LaunchArgs &a) {
     p.n_items = static_cast<int>(items);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.limit_ns = a.limit_ns;
+    p.o_rows = static_cast<long long>(a.BH) * a.N;
+    p.lose_item = -1;
+    p.lose_tile = -1;
+#ifdef FA_DEBUG
+    DebugFault f;
+    if (take_debug_fault(&f)) {
+        if (f.fault == FA_DEBUG_LOSE_K_ARRIVAL) {
+            p.lose_item = f.a > 0x7FFFFFFFLL ? -1 : static_cast<int>(f.a);
+            p.lose_tile = f.b > 0x7FFFFFFFLL ? -1 : static_cast<int>(f.b);
+        } else if (f.fault == FA_DEBUG_SHRINK_OUTPUT) {
+            p.o_rows = f.a < p.o_rows ? f.a : p.o_rows;
+        }
+        if (f.limit_ns) p.limit_ns = f.limit_ns;
+    }
+#endif
     // causal head groups of about two waves of their heaviest items, whole
     // K/V groups, at most all heads (as in the d <= 128 kernel)
     long long hg = (2LL * sms + p.n_qblocks) / (p.n_qblocks + 1);

@@ -58,6 +58,7 @@
 
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
+#include "debug_checks.cuh"
 #ifdef FA_DEBUG
 #include <mutex>
 
@@ -100,33 +101,6 @@ enum : int {
     kSiteSFull, kSiteOFull, kSiteQEmpty, kSiteOEmpty, kSiteSchedFull, kSiteSchedEmpty,
     kSiteClaim
 };
-
-// Device checks of the debug build (compiled with FA_DEBUG).  Every index the
-// kernel computes is checked before use; a failed check records 0x80 | its
-// number in the status word (first error wins), raises the CTA's abort flag
-// and skips the access, so the CTA's other warps stop at their next wait that
-// does not complete at once.  No check traps.  Release builds compile every
-// check to `true`.
-enum : int {
-    kChkItem = 1,  // work item id outside [0, n_items)
-    kChkTmaQ,      // Q box rows outside the padded query rows, or head >= B*H
-    kChkTmaKV,     // K/V box starting at or past N, or K/V head >= B*H_kv
-    kChkSmem,      // a shared-memory range outside the CTA's allocation
-    kChkTmem,      // tensor memory not the whole 512-column allocation
-    kChkStoreO,    // an O store outside the output, or misaligned for its width
-    kChkStoreLse   // an LSE store outside the output
-};
-#ifdef FA_DEBUG
-constexpr bool kDebug = true;
-__device__ __forceinline__ bool dbg_ok(bool cond, const WaitCtl &c, int check) {
-    if (cond) return true;
-    raise_abort(c, 0x80 | check);
-    return false;
-}
-#else
-constexpr bool kDebug = false;
-__device__ __forceinline__ bool dbg_ok(bool, const WaitCtl &, int) { return true; }
-#endif
 
 template <int D>
 struct Cfg {
@@ -244,14 +218,10 @@ __device__ __forceinline__ SmemView<D> smem_view() {
     return v;
 }
 
-// Debug checks: [ptr, ptr + bytes) lies inside the CTA's aligned shared
-// memory, below the 256 KB a descriptor's 14-bit address field reaches.
+// Debug checks: a range inside this kernel's shared memory.
 template <int D>
-__device__ __forceinline__ bool in_smem(const void *ptr, int bytes) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t base = smem_u32(smem_raw), a = smem_u32(ptr);
-    const uint32_t end = base + static_cast<uint32_t>(Cfg<D>::kSmemBytes);
-    return a >= base && a + static_cast<uint32_t>(bytes) <= end && a + bytes <= (1u << 18);
+__device__ __forceinline__ bool in_smem_d(const void *ptr, int bytes) {
+    return in_smem(ptr, bytes, Cfg<D>::kSmemBytes);
 }
 
 // ------------------------------------------------------------- schedule
@@ -353,7 +323,7 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
         }
         if (!dbg_ok(w.bh >= 0 && w.bh < p.BH && w.qb >= 0 && w.qb < p.n_qblocks, ctl,
                     kChkTmaQ) ||
-            !dbg_ok(in_smem<D>(v.q, C::kQBytes), ctl, kChkSmem)) {
+            !dbg_ok(in_smem_d<D>(v.q, C::kQBytes), ctl, kChkSmem)) {
             ok = false;
             break;
         }
@@ -383,8 +353,8 @@ __device__ __forceinline__ void role_producer(const CUtensorMap *tmQ, const CUte
             }
             if (!dbg_ok(j * kBlockN < p.N && w.kvh >= 0 && w.kvh < p.BH / p.group, ctl,
                         kChkTmaKV) ||
-                !dbg_ok(in_smem<D>(v.k + s * C::kTileBytes, C::kTileBytes) &&
-                            in_smem<D>(v.v + s * C::kTileBytes, C::kTileBytes),
+                !dbg_ok(in_smem_d<D>(v.k + s * C::kTileBytes, C::kTileBytes) &&
+                            in_smem_d<D>(v.v + s * C::kTileBytes, C::kTileBytes),
                         ctl, kChkSmem)) {
                 ok = false;
                 g = t;
@@ -457,11 +427,10 @@ __device__ __forceinline__ void role_mma(const Params &p) {
     const int lane = static_cast<int>(threadIdx.x & 31);
     int g = 0;             // K/V tiles consumed, across items
     int pc0 = 0, pc1 = 0;  // P tiles consumed per sub-tile, across items
-    bool ok = dbg_ok((tmem & 0xFFFFu) + kTmemCols <= 512u && (tmem >> 16) == 0u, ctl,
-                     kChkTmem) &&
-              dbg_ok(in_smem<D>(v.q, C::kQBytes) &&
-                         in_smem<D>(v.k, C::kStages * C::kTileBytes) &&
-                         in_smem<D>(v.v, C::kStages * C::kTileBytes),
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem) &&
+              dbg_ok(in_smem_d<D>(v.q, C::kQBytes) &&
+                         in_smem_d<D>(v.k, C::kStages * C::kTileBytes) &&
+                         in_smem_d<D>(v.v, C::kStages * C::kTileBytes),
                      ctl, kChkSmem);
     for (int r = 0; ok; ++r) {
         int x;
@@ -577,8 +546,7 @@ __device__ __forceinline__ void role_softmax(const Params &p, int warp, int lane
     const uint64_t cs2 = f2_pack(cs, cs);
 
     int sc = 0;  // S tiles consumed, across items
-    bool ok = dbg_ok((tmem & 0xFFFFu) + kTmemCols <= 512u && (tmem >> 16) == 0u, ctl,
-                     kChkTmem);
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int r = 0; ok; ++r) {
         int x;
         ok = next_item(v, ctl, r, lane, p.n_items, x);
@@ -806,23 +774,34 @@ __global__ void fa_wait_selftest_kernel(uint64_t limit_ns) {
 }
 
 #ifdef FA_DEBUG
-// The fault fa_debug_arm armed for the next launch (debug build only).
+// The fault fa_debug_arm armed for the next forward launch (debug build
+// only), taken and disarmed by that launch.
 static std::mutex g_arm_mu;
 static int g_arm_fault = FA_DEBUG_NONE;
 static long long g_arm_a = 0, g_arm_b = 0;
 static uint64_t g_arm_limit_ns = 0;
 
-static void take_armed_fault(Params &p) {
+bool take_debug_fault(DebugFault *f) {
     std::lock_guard<std::mutex> lock(g_arm_mu);
-    if (g_arm_fault == FA_DEBUG_NONE) return;
-    if (g_arm_fault == FA_DEBUG_LOSE_K_ARRIVAL) {
-        p.lose_item = g_arm_a > 0x7FFFFFFFLL ? -1 : static_cast<int>(g_arm_a);
-        p.lose_tile = g_arm_b > 0x7FFFFFFFLL ? -1 : static_cast<int>(g_arm_b);
-    } else if (g_arm_fault == FA_DEBUG_SHRINK_OUTPUT) {
-        p.o_rows = g_arm_a < p.o_rows ? g_arm_a : p.o_rows;
-    }
-    if (g_arm_limit_ns) p.limit_ns = g_arm_limit_ns;
+    if (g_arm_fault == FA_DEBUG_NONE) return false;
+    f->fault = g_arm_fault;
+    f->a = g_arm_a;
+    f->b = g_arm_b;
+    f->limit_ns = g_arm_limit_ns;
     g_arm_fault = FA_DEBUG_NONE;
+    return true;
+}
+
+static void take_armed_fault(Params &p) {
+    DebugFault f;
+    if (!take_debug_fault(&f)) return;
+    if (f.fault == FA_DEBUG_LOSE_K_ARRIVAL) {
+        p.lose_item = f.a > 0x7FFFFFFFLL ? -1 : static_cast<int>(f.a);
+        p.lose_tile = f.b > 0x7FFFFFFFLL ? -1 : static_cast<int>(f.b);
+    } else if (f.fault == FA_DEBUG_SHRINK_OUTPUT) {
+        p.o_rows = f.a < p.o_rows ? f.a : p.o_rows;
+    }
+    if (f.limit_ns) p.limit_ns = f.limit_ns;
 }
 #endif
 

@@ -28,6 +28,17 @@ struct LaunchArgs {
 int launch_fwd(const LaunchArgs &a);
 // d = 256 forward (fa_fwd256_sm103.cu).
 int launch_fwd256(const LaunchArgs &a);
+
+#ifdef FA_DEBUG
+// The fault fa_debug_arm (fa_debug.h) armed, if any: taken, and disarmed,
+// by the next forward launch (debug build only).
+struct DebugFault {
+    int fault;
+    long long a, b;
+    uint64_t limit_ns;  // 0: the launch's own limit
+};
+bool take_debug_fault(DebugFault *f);
+#endif
 int fwd256_read_and_clear_status(int *status);
 
 // Backward pass (fa_bwd_sm103.cu).

@@ -18,8 +18,16 @@ from online_softmax_fa_gb300.inputs import make_qkv
 pytestmark = pytest.mark.gpu
 
 SENT_O, SENT_L = 1000.0, -1000.0  # outside any O or LSE these inputs can give
-FWD = 1 << 8  # kernel number of the forward (d 64, 128) in fa_last_device_status
 CHK_STORE_O = 6
+
+
+def kernel_of(d):
+    """The forward kernel's number in fa_last_device_status."""
+    return 2 if d == 256 else 1
+
+
+# each kernel's bounded-wait sites (the numbers it records on a timeout)
+WAIT_SITES = {1: range(1, 14), 2: range(0x41, 0x4F)}
 
 
 @pytest.fixture(scope="module")
@@ -69,6 +77,9 @@ CLEAN_CASES = [
     (1, 1, 1, 1, 128, True, 0),
     (1, 2, 2, 129, 64, True, 8),
     (2, 2, 2, 640, 128, False, 8),
+    (1, 2, 2, 700, 256, True, 0),
+    (2, 4, 2, 333, 256, False, 8),
+    (1, 1, 1, 1, 256, True, 0),
 ]
 
 
@@ -85,9 +96,10 @@ def test_checks_pass_and_match_release(libs, B, H, Hkv, N, d, causal, off):
     assert not (o_d == SENT_O).any()  # every row was written
 
 
-def test_failed_store_check_is_recorded_and_skipped(libs):
+@pytest.mark.parametrize("d", [64, 256])
+def test_failed_store_check_is_recorded_and_skipped(libs, d):
     fa, rel, dbg = libs
-    B, H, N, d = 1, 2, 300, 64
+    B, H, N = 1, 2, 300
     q, k, v = _inputs(B, H, H, N, d, seed=7)
     o_r, l_r = _outputs(q)
     assert _launch(rel, q, k, v, o_r, l_r, False) == 0
@@ -97,7 +109,7 @@ def test_failed_store_check_is_recorded_and_skipped(libs):
     assert dbg.fa_debug_arm(fa.FA_DEBUG_SHRINK_OUTPUT, rows - 1, 0, 20000) == 0
     o, lse = _outputs(q)
     assert _launch(dbg, q, k, v, o, lse, False) == fa.FA_ERR_CHECK
-    assert dbg.fa_last_device_status() == FWD | 0x80 | CHK_STORE_O
+    assert dbg.fa_last_device_status() == (kernel_of(d) << 8) | 0x80 | CHK_STORE_O
     assert (o[0, 1, N - 1] == SENT_O).all() and lse[0, 1, N - 1] == SENT_L
     # every other row holds the release result, or the sentinel where the
     # aborted CTA stopped early
@@ -115,22 +127,24 @@ def test_failed_store_check_is_recorded_and_skipped(libs):
     assert torch.equal(o, o_r) and torch.equal(lse, l_r)
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_lost_arrival_times_out_and_context_survives(libs, causal):
+def test_lost_arrival_times_out_and_context_survives(libs, causal, d):
     fa, rel, dbg = libs
-    B, H, N, d = 1, 2, 1024, 128
+    B, H, N = 1, 2, 1024
     q, k, v = _inputs(B, H, H, N, d, seed=9)
     o_r, l_r = _outputs(q)
     assert _launch(rel, q, k, v, o_r, l_r, causal) == 0
-    # work item 0 (the first CTA's own, 8 key tiles long in both orders)
-    # loses the arrival of its key tile 1; every wait is limited to 20 ms
+    # work item 0 (the first CTA's own, 8 key tiles long in both orders and
+    # at both head dimensions) loses the arrival of its key tile 1; every
+    # wait is limited to 20 ms
     assert dbg.fa_debug_arm(fa.FA_DEBUG_LOSE_K_ARRIVAL, 0, 1, 20000) == 0
     o, lse = _outputs(q)
     t0 = time.monotonic()
     assert _launch(dbg, q, k, v, o, lse, causal) == fa.FA_ERR_TIMEOUT
     assert time.monotonic() - t0 < 10.0
     st = dbg.fa_last_device_status()
-    assert st >> 8 == 1 and 1 <= (st & 0xFF) <= 13, hex(st)  # a forward wait ran out
+    assert st >> 8 == kernel_of(d) and (st & 0xFF) in WAIT_SITES[st >> 8], hex(st)
     assert dbg.fa_device_error(None) == 0  # cleared
     # the context is usable: a clean launch of both builds matches
     o, lse = _outputs(q)
