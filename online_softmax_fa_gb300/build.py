@@ -5,7 +5,7 @@ one nvcc call links the shared library.  No CMake, no torch extension
 machinery: the library exports the plain C ABI of ``include/fa.h``.
 
 The same call builds the debug library ``_build/libfa_gb300_debug.so``: the
-release objects with the forward kernels' units recompiled with ``FA_DEBUG``
+release objects with the attention kernels' units recompiled with ``FA_DEBUG``
 (device index checks and the fault knobs of ``include/fa_debug.h``).
 """
 from __future__ import annotations
@@ -21,7 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300.so")
 DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300_debug.so")
-DEBUG_SOURCES = ["fa_fwd_sm103.cu", "fa_fwd256_sm103.cu"]  # recompiled with FA_DEBUG
+# recompiled with FA_DEBUG for the debug library
+DEBUG_SOURCES = ["fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu", "fa_bwd256_sm103.cu"]
 SOURCES = ["fa_api.cu", "fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu",
            "fa_bwd256_sm103.cu", "fa_decode_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

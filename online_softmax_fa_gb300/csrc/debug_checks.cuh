@@ -1,5 +1,5 @@
 // debug_checks.cuh -- device checks of the debug build (compiled with
-// FA_DEBUG) of the forward kernels.  Every index a kernel computes is
+// FA_DEBUG) of the forward and backward kernels.  Every index a kernel computes is
 // checked before use; a failed check records 0x80 | its number in the
 // kernel's status word (first error wins), raises the CTA's abort flag and
 // skips the access, so the CTA's other warps stop at their next wait that
@@ -28,9 +28,17 @@ __device__ __forceinline__ bool dbg_ok(bool cond, const WaitCtl &c, int check) {
     raise_abort(c, 0x80 | check);
     return false;
 }
+// The same for a kernel without bounded waits: records the failure in
+// `status` only.
+__device__ __forceinline__ bool dbg_ok_word(bool cond, int *status, int check) {
+    if (cond) return true;
+    atomicCAS(status, 0, 0x80 | check);
+    return false;
+}
 #else
 constexpr bool kDebug = false;
 __device__ __forceinline__ bool dbg_ok(bool, const WaitCtl &, int) { return true; }
+__device__ __forceinline__ bool dbg_ok_word(bool, int *, int) { return true; }
 #endif
 
 // [ptr, ptr + bytes) lies inside the CTA's dynamic shared memory of

@@ -45,6 +45,7 @@
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 #include "bwd_elementwise.cuh"
+#include "debug_checks.cuh"
 
 namespace fa {
 
@@ -296,6 +297,10 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQh, const CUt
     const int i0 = CAUSAL ? jb : 0;
     const int n_q = p.n_blocks - i0;
     const int n_u = 2 * p.group * n_q;
+    if (!dbg_ok(bh >= 0 && bh < p.grid_heads && jb >= 0 && jb < p.n_blocks &&
+                    in_smem(v.c(0), kRegions * kRegion, kSmemBytes),
+                ctl, kChkItem))
+        return;
     const uint64_t pol = l2_policy_evict_last();
     mbar_arrive_expect_tx(v.once, DV ? kTile : 2 * kTile);
     if (!DV) load_rows(v.c(0), kBox, tmV, v.once, jb * kBlk, bh, pol);  // V_j, resident
@@ -309,6 +314,13 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQh, const CUt
         const int bq = q_head(p, bh, g);
         const size_t prow = static_cast<size_t>(bq) * p.n_blocks * kBlk + qr;
         float *rows = v.rows(r);
+        if (!dbg_ok(bq >= 0 && bq < p.grid_heads * p.group && qr >= 0 &&
+                        qr < p.n_blocks * kBlk &&
+                        prow + kHalf <= static_cast<size_t>(p.grid_heads) * p.group *
+                                            p.n_blocks * kBlk,
+                    ctl, kChkTmaQ) ||
+            !dbg_ok(in_smem(rows, 2 * kHalf * 4, kSmemBytes), ctl, kChkSmem))
+            break;
         mbar_arrive_expect_tx(&v.full[s], 2 * kHTile + (DV ? 1 : 2) * kHalf * 4);
         load_rows(v.c(r), kHBox, tmQh, &v.full[s], qr, bq, pol);
         load_rows(v.e(r), kHBox, tmdOh, &v.full[s], qr, bq, pol);
@@ -329,7 +341,7 @@ __device__ __forceinline__ void dkdv_mma(const Params &p, int jb) {
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    bool ok = wait(v.once, 0, kSiteOnce);
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem) && wait(v.once, 0, kSiteOnce);
     if (ok) ok = stage_to_tmem<S>(v, tmem, ctl);  // K_j
     if (DV) {
         // S^T(u + 1) into the other buffer before dV(u): the buffer last
@@ -400,7 +412,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
     const auto wait = [&](uint64_t *bar, uint32_t par, int site) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int u = 0; u < n_u && ok; ++u) {
         const float *rows = v.rows(region_of<S>(u)) + 32 * c;
         ok = wait(&v.full[u % S], (u / S) & 1, kSiteFull);  // the half's statistics
@@ -462,7 +474,10 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int bh, int jb
             for (int e = 0; e < 16; ++e)
                 pa[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
                                     __uint_as_float(a[2 * e + 1]) * mul);
-            if (in) {
+            if (in && dbg_ok(static_cast<size_t>(bh) * N + key <
+                                     static_cast<size_t>(p.grid_heads) * N &&
+                                 (reinterpret_cast<uintptr_t>(dst + 32 * g) & 15u) == 0,
+                             ctl, kChkStoreO)) {
                 uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * g);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -530,6 +545,10 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd256, p.limit_ns};
     const int n_u = 2 * (CAUSAL ? ib + 1 : p.n_blocks);
     const int bk = kv_head(p, bh);
+    if (!dbg_ok(bh >= 0 && bh < p.grid_heads && ib >= 0 && ib < p.n_blocks &&
+                    in_smem(v.c(0), kRegions * kRegion, kSmemBytes),
+                ctl, kChkItem))
+        return;
     const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(v.once, 2 * kTile);
     load_rows(v.c(0), kBox, tmdO, v.once, ib * kBlk, bh, pol_q);             // dO_i, resident
@@ -538,6 +557,9 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     for (int u = 0; u < n_u; ++u) {
         if (!wait_stage_free<2>(v, u, ctl)) break;
         const int s = u & 1, r = region_of<2>(u);
+        if (!dbg_ok(u * kHalf < p.n_blocks * kBlk && bk >= 0 && bk < p.grid_heads / p.group,
+                    ctl, kChkTmaKV))
+            break;
         mbar_arrive_expect_tx(&v.full[s], 2 * kHTile);
         load_rows(v.c(r), kHBox, tmKh, &v.full[s], u * kHalf, bk, pol_kv);
         load_rows(v.e(r), kHBox, tmVh, &v.full[s], u * kHalf, bk, pol_kv);
@@ -556,7 +578,7 @@ __device__ __forceinline__ void dq_mma(const Params &p, int ib) {
         return __all_sync(0xffffffffu, mbar_wait(bar, par, ctl, site));
     };
     const uint64_t ddO = sdesc_sw128(smem_u32(v.c(0)), 16, 1024);
-    bool ok = wait(v.once, 0, kSiteOnce);
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem) && wait(v.once, 0, kSiteOnce);
     if (ok) ok = stage_to_tmem<2>(v, tmem, ctl);  // Q_i
     for (int u = 0; u < n_u && ok; ++u) {
         const int s = u & 1, r = region_of<2>(u);
@@ -592,7 +614,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
     const size_t prow = static_cast<size_t>(bh) * p.n_blocks * kBlk + q;  // padded row
     const float my_nl2 = p.lse2[prow], my_nd = p.dd[prow];
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int u = 0; u < n_u && ok; ++u) {
         ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[0], u & 1, ctl, kSiteS));
         if (!ok) break;
@@ -630,7 +652,10 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int bh, int ib, 
             for (int e = 0; e < 16; ++e)
                 pa[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale,
                                     __uint_as_float(a[2 * e + 1]) * p.scale);
-            if (in) {
+            if (in && dbg_ok(static_cast<size_t>(bh) * N + q <
+                                     static_cast<size_t>(p.grid_heads) * N &&
+                                 (reinterpret_cast<uintptr_t>(dq + 32 * g) & 15u) == 0,
+                             ctl, kChkStoreO)) {
                 uint4 *o = reinterpret_cast<uint4 *>(dq + 32 * g);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)

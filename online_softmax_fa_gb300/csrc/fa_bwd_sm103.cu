@@ -45,6 +45,7 @@
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
 #include "bwd_elementwise.cuh"
+#include "debug_checks.cuh"
 
 namespace fa {
 
@@ -290,7 +291,10 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
     // head's group in turn, per query block Q_i, dO_i (TMA) and the block's
     // LSE2 and D rows (bulk copies of the padded rows), all completing the
     // stage's barrier
-    if (lane == 0) {
+    if (lane == 0 &&
+        dbg_ok(bh >= 0 && bh < p.grid_heads && jb >= 0 && jb < p.n_blocks &&
+                   in_smem(v.a, 2 * C::kTile, C::kSmemBytes),
+               ctl, kChkItem)) {
         const uint64_t pol = l2_policy_evict_last();
         mbar_arrive_expect_tx(v.once, 2 * C::kTile);
         load_tile<D>(v.a, tmK, v.once, jb * kBlk, bh, pol);
@@ -308,6 +312,15 @@ __device__ __forceinline__ void dkdv_producer(const CUtensorMap *tmQ, const CUte
             const size_t prow = static_cast<size_t>(bq) * p.n_blocks * kBlk;
             float *lse2 = v.rows + s * 2 * kBlk, *dd = lse2 + kBlk;
             uint8_t *st = v.ring + s * 2 * C::kTile;
+            if (!dbg_ok(bq >= 0 && bq < p.BH && q0 >= 0 && q0 < p.n_blocks * kBlk &&
+                            prow + q0 + kBlk <= static_cast<size_t>(p.BH) * p.n_blocks * kBlk,
+                        ctl, kChkTmaQ) ||
+                !dbg_ok(in_smem(st, 2 * C::kTile, C::kSmemBytes) &&
+                            in_smem(lse2, 2 * kBlk * 4, C::kSmemBytes),
+                        ctl, kChkSmem)) {
+                ok = false;
+                break;
+            }
             mbar_arrive_expect_tx(&v.full[s], 2 * C::kTile + 2 * kBlk * 4);
             load_tile<D>(st, tmQ, &v.full[s], q0, bq, pol);
             load_tile<D>(st + C::kTile, tmdO, &v.full[s], q0, bq, pol);
@@ -356,7 +369,7 @@ __device__ __forceinline__ void dkdv_issue_sdp(const Params &p) {
     const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
     const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);
     uint64_t *buf_free = v.vfull;
-    bool ok = wait(v.once, 0, kSiteKV);
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem) && wait(v.once, 0, kSiteKV);
     for (int u = 0; u < n_u && ok; ++u) {
         const int t = u >> 1;
         if ((u & 1) == 0) {
@@ -397,7 +410,7 @@ __device__ __forceinline__ void dkdv_issue_acc(const Params &p) {
     const uint64_t to = static_cast<uint64_t>(C::kTile >> 4);
     const uint64_t ho = static_cast<uint64_t>((64 * 128) >> 4);
     uint64_t *buf_free = v.vfull;
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int u = 0; u < n_u && ok; ++u) {
         ok = wait(&v.p_full[u & 1], (u >> 1) & 1, kSiteP);
         if (!ok) break;
@@ -433,7 +446,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
     const int row = quarter * 32 + lane;
     const int key = jb * kBlk + row;
     const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int u = 0; u < n_u && ok; ++u) {
         const int t = u >> 1, h = u & 1, s = t % C::kStages;
         // the stage's LSE2/D rows landed with its tiles (the stage cannot
@@ -481,6 +494,7 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
     if (ok) {
         tc_fence_after();
         const bool in = key < N;
+        const bool row_ok = static_cast<size_t>(bh) * N + key < static_cast<size_t>(p.grid_heads) * N;
         __nv_bfloat16 *dvp = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
         __nv_bfloat16 *dkp = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
 #pragma unroll 1
@@ -494,7 +508,9 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
                 pb[e] = pack_bf16x2(__uint_as_float(b[2 * e]) * p.scale,
                                     __uint_as_float(b[2 * e + 1]) * p.scale);
             }
-            if (in) {
+            if (in && dbg_ok(row_ok && ((reinterpret_cast<uintptr_t>(dvp + 32 * g) |
+                                         reinterpret_cast<uintptr_t>(dkp + 32 * g)) & 15u) == 0,
+                             ctl, kChkStoreO)) {
                 uint4 *o0 = reinterpret_cast<uint4 *>(dvp + 32 * g);
                 uint4 *o1 = reinterpret_cast<uint4 *>(dkp + 32 * g);
 #pragma unroll
@@ -564,7 +580,10 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
     const WaitCtl ctl{v.abort_flag, &g_fa_status_bwd, p.limit_ns};
     (void)N, (void)tmem, (void)bh;
     const int bk = kv_head(p, bh);  // this query head's K/V head
-    if (lane == 0) {
+    if (lane == 0 &&
+        dbg_ok(bh >= 0 && bh < p.grid_heads && ib >= 0 && ib < p.n_blocks &&
+                   in_smem(v.a, 2 * C::kTile, C::kSmemBytes),
+               ctl, kChkItem)) {
         const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
         mbar_arrive_expect_tx(v.once, 2 * C::kTile);
         load_tile<D>(v.a, tmQ, v.once, ib * kBlk, bh, pol_q);
@@ -576,6 +595,14 @@ __device__ __forceinline__ void dq_producer(const CUtensorMap *tmQ, const CUtens
             if (t >= C::kStagesK)
                 ok = mbar_wait(&v.empty[sk], ((t / C::kStagesK) & 1) ^ 1, ctl, kSiteEmpty);
             if (!ok) break;
+            if (!dbg_ok(t * kBlk < p.n_blocks * kBlk && bk >= 0 && bk < p.BH / p.group, ctl,
+                        kChkTmaKV) ||
+                !dbg_ok(in_smem(v.ring + sk * C::kTile, C::kTile, C::kSmemBytes) &&
+                            in_smem(v.vring + sv * C::kTile, C::kTile, C::kSmemBytes),
+                        ctl, kChkSmem)) {
+                ok = false;
+                break;
+            }
             mbar_arrive_expect_tx(&v.full[sk], C::kTile);
             load_tile<D>(v.ring + sk * C::kTile, tmK, &v.full[sk], t * kBlk, bk, pol_kv);
             ++nk;
@@ -624,7 +651,7 @@ __device__ __forceinline__ void dq_mma(const Params &p) {
     // pipe while the elementwise warps work on block t: S(t+1) as soon as
     // K(t+1) is in (its buffer held dS(t-1), read by dQ(t-1) issued before),
     // dP(t+1) once the warps have read dP(t) (dp_free).
-    bool ok = wait(v.once, 0, kSiteKV);
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem) && wait(v.once, 0, kSiteKV);
     if (ok) ok = wait(&v.full[0], 0, kSiteQ);
     if (ok) ok = wait(&v.vfull[0], 0, kSiteQ);
     if (ok) {
@@ -683,7 +710,7 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
     const size_t prow = static_cast<size_t>(bh) * p.n_blocks * kBlk + q;  // padded row
     const float my_nl2 = p.lse2[prow];  // -LSE log2 e (zero past N)
     const float my_nd = p.dd[prow];     // -D
-    bool ok = true;
+    bool ok = dbg_ok(whole_tmem(tmem), ctl, kChkTmem);
     for (int t = 0; t < n_k && ok; ++t) {
         ok = __all_sync(0xffffffffu, mbar_wait(&v.s_full[t & 1], (t >> 1) & 1, ctl, kSiteS));
         if (!ok) break;
@@ -729,7 +756,9 @@ __device__ __forceinline__ void dq_elementwise(const Params &p, int warp, int la
             for (int t = 0; t < 16; ++t)
                 pa[t] = pack_bf16x2(__uint_as_float(a[2 * t]) * p.scale,
                                     __uint_as_float(a[2 * t + 1]) * p.scale);
-            if (qin) {
+            if (qin && dbg_ok(static_cast<size_t>(bh) * N + q < static_cast<size_t>(p.BH) * N &&
+                                  (reinterpret_cast<uintptr_t>(dq + 32 * c) & 15u) == 0,
+                              ctl, kChkStoreO)) {
                 uint4 *o = reinterpret_cast<uint4 *>(dq + 32 * c);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)
@@ -814,7 +843,8 @@ __global__ void pre_kernel(const __nv_bfloat16 *__restrict__ O,
         }
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (c == 0) {
+        if (c == 0 && dbg_ok_word(prow < rows_pad && bh * Npad + q == prow, &g_fa_status_bwd,
+                                  kChkStoreLse)) {
             dd[prow] = -acc;
             lse2[prow] = q < N ? -LSE[bh * N + q] * kLog2e : 0.f;
         }

@@ -1,7 +1,7 @@
 """The debug build (include/fa_debug.h) on the GPU.
 
-- Its device index checks pass on valid requests, and its output is
-  bit-identical to the release build's.
+- Its device index checks (forward and backward kernels) pass on valid
+  requests, and its outputs are bit-identical to the release build's.
 - A failed check is recorded (FA_ERR_CHECK, with the check's number) and its
   store skipped.  The fault shrinks the extent that the checks use, so every
   skipped store lay inside the real buffer.
@@ -153,3 +153,41 @@ def test_lost_arrival_times_out_and_context_survives(libs, causal, d):
     o2, l2 = _outputs(q)
     assert _launch(rel, q, k, v, o2, l2, causal) == 0
     assert torch.equal(o2, o_r)
+
+
+BWD_CASES = [
+    # B, H, H_kv, N, d, causal
+    (1, 2, 2, 300, 64, True),
+    (1, 4, 2, 640, 128, False),
+    (2, 2, 2, 129, 128, True),
+    (1, 1, 1, 1, 128, True),
+    (1, 2, 1, 333, 256, True),
+    (1, 2, 2, 256, 256, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal", BWD_CASES)
+def test_backward_checks_pass_and_match_release(libs, B, H, Hkv, N, d, causal):
+    """The backward kernels' checks (debug build) pass, and the gradients are
+    bit-identical to the release build's."""
+    fa, rel, dbg = libs
+    q, k, v = _inputs(B, H, Hkv, N, d, seed=80 + N)
+    o, lse = _outputs(q)
+    assert _launch(rel, q, k, v, o, lse, causal) == 0
+    g = torch.Generator(device="cpu").manual_seed(81 + N)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(q.device)
+    stream = torch.cuda.current_stream().cuda_stream
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    got = []
+    for lib in (rel, dbg):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        rc = lib.fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), ws.data_ptr(), ws.numel(), B, H, Hkv, N, d,
+                            int(causal), float(d) ** -0.5, stream)
+        assert rc == 0
+        assert lib.fa_device_error(stream) == 0
+        got.append((dq, dk, dv))
+    assert dbg.fa_last_device_status() == 0
+    for a, b in zip(*got):
+        assert torch.equal(a, b)
