@@ -3,28 +3,29 @@
  * (_build/libfa_gb300_debug.so, the attention kernels compiled with FA_DEBUG).
  *
  * The debug build exports everything fa.h declares and behaves like the
- * release build, with one difference: the forward and backward kernels
- * (head dimensions 64, 128 and 256) check each index they compute before
- * using it:
+ * release build, with one difference: the forward, backward and decoding
+ * kernels (head dimensions 64, 128 and 256) check each index they compute
+ * before using it:
  *   - the work item id (from the grid or a cancelled CTA) or the CTA's
  *     (head, block);
  *   - the head and row coordinates of every Q, K, V and dO tensor-map load
- *     and of every bulk copy of the backward's row statistics;
+ *     and of every bulk copy of the backward's row statistics, and the query
+ *     rows decoding reads;
  *   - the shared-memory ranges that the loads write and the MMAs read;
  *   - the tensor-memory allocation;
- *   - the element range and alignment of every O, dQ, dK and dV store, and
- *     the index of every LSE (and backward statistics) store.
+ *   - the element range and alignment of every O, dQ, dK and dV store, the
+ *     index of every LSE (and backward statistics) store, and the slot of
+ *     every partial decoding state written and merged.
  * A failed check writes 0x80 | its number to the kernel's device status
  * word; the first error wins.  The access is skipped, and the CTA's abort
  * flag is raised so the CTA's other warps stop at their next wait.  No
  * check traps.  fa_device_error then returns FA_ERR_CHECK, and
  * fa_last_device_status returns (k << 8) | 0x80 | n, with k the kernel
  * number of fa.h (1 forward d 64/128, 2 forward d 256, 3 backward d 64/128,
- * 4 backward d 256), and n:
+ * 4 backward d 256, 5 decoding), and n:
  *   1 item id, 2 Q (dO) load, 3 K/V load, 4 shared memory, 5 tensor
  *   memory, 6 O (dQ, dK, dV) store, 7 LSE (statistics) store.
- * The decoding kernels are the release code.  The fault knobs below apply
- * to the forward kernels.
+ * The fault knobs below apply to the forward kernels.
  * The checks follow the kernel's own design: one CTA per
  * (batch, head, query block) work item, tiled over key blocks
  * ("Understanding FlashAttention Pt 1" (wpnews.pro), section 2.4, and

@@ -22,7 +22,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300.so")
 DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libfa_gb300_debug.so")
 # recompiled with FA_DEBUG for the debug library
-DEBUG_SOURCES = ["fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu", "fa_bwd256_sm103.cu"]
+DEBUG_SOURCES = ["fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu", "fa_bwd256_sm103.cu",
+                 "fa_decode_sm103.cu"]
 SOURCES = ["fa_api.cu", "fa_fwd_sm103.cu", "fa_fwd256_sm103.cu", "fa_bwd_sm103.cu",
            "fa_bwd256_sm103.cu", "fa_decode_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,5 +1,5 @@
 // debug_checks.cuh -- device checks of the debug build (compiled with
-// FA_DEBUG) of the forward and backward kernels.  Every index a kernel computes is
+// FA_DEBUG) of the attention kernels.  Every index a kernel computes is
 // checked before use; a failed check records 0x80 | its number in the
 // kernel's status word (first error wins), raises the CTA's abort flag and
 // skips the access, so the CTA's other warps stop at their next wait that
@@ -49,6 +49,13 @@ __device__ __forceinline__ bool in_smem(const void *ptr, int bytes, int smem_byt
     const uint32_t base = smem_u32(smem_raw), a = smem_u32(ptr);
     const uint32_t end = base + static_cast<uint32_t>(smem_bytes);
     return a >= base && a + static_cast<uint32_t>(bytes) <= end && a + bytes <= (1u << 18);
+}
+
+// The same against a kernel's own aligned dynamic shared-memory base.
+__device__ __forceinline__ bool in_smem_at(const void *base, const void *ptr, int bytes,
+                                           int smem_bytes) {
+    const uint32_t b = smem_u32(base), a = smem_u32(ptr);
+    return a >= b && a + static_cast<uint32_t>(bytes) <= b + static_cast<uint32_t>(smem_bytes);
 }
 
 // The TMEM address of a whole 512-column allocation starts at lane 0,

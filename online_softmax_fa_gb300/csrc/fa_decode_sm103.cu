@@ -35,6 +35,7 @@
 
 #include "fa_internal.h"
 #include "sm103_primitives.cuh"
+#include "debug_checks.cuh"
 
 namespace fa {
 
@@ -181,6 +182,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (i >= S) ok = mbar_wait(&empty[s], static_cast<uint32_t>((i / S) & 1) ^ 1u, ctl, 1);
             if (!ok) break;
             uint8_t *dst = smem + C::kOffRing + s * 2 * C::kTileBytes;
+            if (!dbg_ok(h >= 0 && h < n_heads && j >= 0 && j < T_h, ctl, kChkTmaKV) ||
+                !dbg_ok(in_smem_at(smem, dst, 2 * C::kTileBytes, C::kSmemBytes - 128), ctl,
+                        kChkSmem)) {
+                ok = false;
+                break;
+            }
             mbar_arrive_expect_tx(&full[s], 2 * C::kTileBytes);
             for (int r = 0; r < C::kTileKeys; r += 64) {  // 64-row boxes
                 tma_load_3d(dst + r * D * 2, &tmK, &full[s], 0, j * C::kTileKeys + r, h, pol);
@@ -263,6 +270,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (!meet()) return false;
         const long long hT = static_cast<long long>(h) * T_h;
         const int slot = c - dec_cta_of(hT, T, grid);
+        if (!dbg_ok(h >= 0 && h < n_heads && slot >= 0 && slot < stride, ctl, kChkStoreO))
+            return false;
         for (int q = ctid; q < G * D; q += kDecConsumers * 32) {
             const int g = q / D, dim = q - g * D;  // query head g of the group
             const int gw = g / GW, gl = g - gw * GW;  // its head group, index there
@@ -306,6 +315,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             cur = h;
             const int b = h / H_kv, kvh = h - b * H_kv;
+            if (!dbg_ok(h < n_heads && kvh * G + hg * GW + GW <= H, ctl, kChkTmaQ)) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int g = 0; g < GW; ++g) {
                 const uint4 qq = *reinterpret_cast<const uint4 *>(
@@ -445,7 +458,8 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     const int bkv = b * H_kv + kvh;
     const long long T = static_cast<long long>(rows / H) * H_kv * T_h;
     const long long first = static_cast<long long>(bkv) * T_h;
-    const int n_slots = dec_cta_of(first + T_h - 1, T, grid) - dec_cta_of(first, T, grid) + 1;
+    int n_slots = dec_cta_of(first + T_h - 1, T, grid) - dec_cta_of(first, T, grid) + 1;
+    if (!dbg_ok_word(n_slots >= 1 && n_slots <= stride, &g_fa_status_dec, kChkItem)) n_slots = 0;
     const size_t base = static_cast<size_t>(bkv) * stride;
     float M = -INFINITY;
     for (int s = lane; s < n_slots; s += 32) M = fmaxf(M, part_ml[((base + s) * G + g) * 2]);

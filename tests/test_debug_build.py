@@ -191,3 +191,39 @@ def test_backward_checks_pass_and_match_release(libs, B, H, Hkv, N, d, causal):
     assert dbg.fa_last_device_status() == 0
     for a, b in zip(*got):
         assert torch.equal(a, b)
+
+
+DEC_CASES = [
+    # B, H, H_kv, N, d
+    (2, 8, 2, 1000, 128),
+    (1, 4, 4, 100, 64),
+    (2, 8, 1, 4097, 256),
+    (3, 16, 2, 1, 128),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d", DEC_CASES)
+def test_decode_checks_pass_and_match_release(libs, B, H, Hkv, N, d):
+    """The decoding kernels' checks (debug build) pass, and the output is
+    bit-identical to the release build's."""
+    fa, rel, dbg = libs
+    dev = torch.device("cuda")
+    g = torch.Generator(device="cpu").manual_seed(90 + N)
+    q = torch.randn(B, H, d, generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn(B, Hkv, N, d, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(B, Hkv, N, d, generator=g).to(torch.bfloat16).to(dev)
+    need = fa.fa_decode_workspace_bytes(B, H, Hkv, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    got = []
+    for lib in (rel, dbg):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        rc = lib.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), ws.data_ptr(), need, B, H, Hkv, N, d,
+                           float(d) ** -0.5, stream)
+        assert rc == 0
+        assert lib.fa_device_error(stream) == 0
+        got.append((o, lse))
+    assert dbg.fa_last_device_status() == 0
+    assert torch.equal(got[0][0], got[1][0]) and torch.equal(got[0][1], got[1][1])
