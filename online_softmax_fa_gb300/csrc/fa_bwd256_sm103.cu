@@ -34,8 +34,9 @@
 //     keys.  TMEM: S [0, 64), dP [64, 128), Q_i [128, 256), dQ [256, 512).
 // In the dK CTA and in dQ, TMEM holds one S^T / dP^T (S / dP) pair, so a
 // half's MMAs wait for the elementwise step of the previous half.  The
-// kernels are deterministic (no atomics, fixed order).  Causal: blocks above the diagonal are skipped, the
-// diagonal block and a ragged last block masked per element.
+// kernels are deterministic (no atomics, fixed order).  Causal: blocks above
+// the diagonal are skipped, the diagonal block and a ragged last block
+// masked per element.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -494,7 +494,8 @@ __device__ __forceinline__ void dkdv_elementwise(const Params &p, int warp, int 
     if (ok) {
         tc_fence_after();
         const bool in = key < N;
-        const bool row_ok = static_cast<size_t>(bh) * N + key < static_cast<size_t>(p.grid_heads) * N;
+        const bool row_ok =
+            static_cast<size_t>(bh) * N + key < static_cast<size_t>(p.grid_heads) * N;
         __nv_bfloat16 *dvp = p.g1 + (static_cast<size_t>(bh) * N + key) * D;
         __nv_bfloat16 *dkp = p.g0 + (static_cast<size_t>(bh) * N + key) * D;
 #pragma unroll 1
